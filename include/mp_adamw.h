@@ -1,0 +1,207 @@
+/*
+ * mp_adamw.h — C ABI of libmpadamw.so: the mixed-precision optimizer step of
+ * bf16 LLM training on one GB300 (sm_103a).
+ *
+ * Sources (web pages; cited by title and section):
+ *   [LLMC]  llm.c code walk-through, ch. 04 "Multi-GPU and mixed precision"
+ *           (ai-reference-codex.pages.dev): §2.1 precision table, §2.2 AdamW
+ *           kernel, §2.3 stochastic rounding, §3.2 ZeRO-1 shards, §4 train step.
+ *   [CMU13] CMU 11-667 lecture 13 notes, "Scaling up LLMs: optimization and
+ *           parallel training" (semidirectx.com): §1.6-1.7 Adam/AdamW details,
+ *           §2.3 fp32 master weights, §7.3 exercises 1 and 5.
+ *   [DIST3] "LLM distributed training: CUDA/ROCm multi-GPU, part 3": §3.1
+ *           ZeRO stage 1 (the shard is a contiguous index range).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - bf16 values travel as their raw 16-bit patterns (uint16_t).
+ *  - Every pointer is a DEVICE pointer unless marked "host". The caller owns
+ *    every buffer and the stream; the library keeps no pointer after return.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Every call only enqueues work on `stream` and returns; nothing here
+ *    synchronises the device or the stream.
+ *  - Calls validate their arguments on the host before any launch. On an
+ *    error they return a status != MP_OK and enqueue nothing: no output
+ *    buffer is touched.
+ *  - Element counts and offsets are 64-bit: a parameter set may exceed 2^32
+ *    elements. A "global index" is an element's position in the whole flat
+ *    parameter buffer; a call may cover only the range
+ *    [global_offset, global_offset + n) of it (a ZeRO-1 shard, [LLMC] §3.2,
+ *    [DIST3] §3.1), and every pointer then addresses element global_offset.
+ *  - Pointers must be aligned to their element size (2 B for bf16, 4 B for
+ *    fp32, 8 B for fp64) or the call returns MP_ERR_ALIGN. Buffers that are
+ *    also 16-B aligned take the vectorised kernels; others take scalar
+ *    kernels that compute bit-identical results more slowly.
+ *  - Nothing in the library calls exit(), prints, or allocates device memory.
+ */
+#ifndef MP_ADAMW_H
+#define MP_ADAMW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MP_ABI_VERSION 1
+
+/* One tensor of the flat parameter buffer. Offsets and sizes are global
+ * element indices. `decay` is 1 for tensors that take weight decay and 0 for
+ * those that do not; [LLMC] §2.2 decays embeddings and matrices (2D tensors)
+ * and exempts LayerNorm weights and biases (1D tensors). */
+typedef struct mp_tensor {
+    uint64_t offset;
+    uint64_t size;
+    int32_t decay;
+    int32_t reserved; /* must be 0 */
+} mp_tensor_t;
+
+typedef enum mp_status {
+    MP_OK = 0,
+    MP_ERR_NULL = 1,      /* a required pointer is NULL                          */
+    MP_ERR_ALIGN = 2,     /* a pointer is not aligned to its element size        */
+    MP_ERR_TABLE = 3,     /* tensor table malformed or not covering the range   */
+    MP_ERR_RANGE = 4,     /* a size, step or hyperparameter is out of range      */
+    MP_ERR_NONFINITE = 5, /* device-reported: the clip scale was NaN or Inf      */
+    MP_ERR_CUDA = 6,      /* a CUDA runtime call failed (see mp_last_cuda_error) */
+    MP_ERR_WORKSPACE = 7  /* workspace missing or smaller than required          */
+} mp_status_t;
+
+/* ABI version this library was built with (MP_ABI_VERSION). */
+int mp_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mp_status_string(int status);
+
+/* The cudaError_t of the last failing CUDA call made by the calling host
+ * thread inside this library, 0 if none. Thread-local. */
+int mp_last_cuda_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Gradient norm and clip scale — [LLMC] §4 ("grad_norm = global norm";
+ * "grad_scale = min(1, 1.0/grad_norm)", i.e. clipping to norm 1.0).
+ *
+ *   sumsq = sum over all i < n of (float)grads[i]^2    (all tensors, 1D too)
+ *   norm  = (float) sqrt(sumsq)
+ *   scale = NaN                        if norm is NaN or Inf
+ *         = min(1, clip / norm)        otherwise (fp32 divide; norm 0 -> 1)
+ *
+ * The kernel squares in fp32 (exact for |g| in [2^-63, 2^64)), sums each
+ * thread's terms with compensation, and reduces across threads and blocks in
+ * fp64 in a fixed order; a block whose fp32 partial is non-finite or below
+ * 2^-60 recomputes its share in fp64. The result is bit-identical on every
+ * run with the same n on the same GPU model; its relative error against an
+ * fp64 sum is below 1e-6 for any finite input.
+ *
+ *   grads       bf16[n], device, read only.
+ *   n           element count; 0 gives sumsq 0, norm 0, scale 1.
+ *   clip        clip threshold, finite and > 0 (the train step uses 1.0).
+ *   workspace   device scratch of at least mp_grad_norm_workspace_bytes(n)
+ *               bytes, 8-B aligned; overwritten, no initial contents needed;
+ *               must not be shared with another call in flight.
+ *   d_norm      float[1], device, written.
+ *   d_scale     float[1], device, written (feeds mp_adamw_step).
+ *   d_sumsq     double[1], device, written; may be NULL.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE (clip), MP_ERR_WORKSPACE,
+ *         MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t mp_grad_norm_workspace_bytes(uint64_t n);
+
+int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip,
+                 void* workspace, size_t workspace_bytes,
+                 float* d_norm, float* d_scale, double* d_sumsq,
+                 void* stream);
+
+/* ---------------------------------------------------------------------------
+ * AdamW step with stochastic-rounding write-back — [LLMC] §2.2 (update),
+ * §2.3 (rounding), §4 (t = step + 1); [CMU13] §1.7 (bias correction,
+ * decoupled decay).
+ *
+ * Host side: bc1 = (float)(1 - beta1^t), bc2 = (float)(1 - beta2^t), both
+ * computed in double and rounded once. Per element i in the range, in fp32
+ * with round-to-nearest-even, no FMA contraction except the two lerps, and
+ * no flush of subnormals:
+ *
+ *   g    = scale * (float)grads[i]
+ *   m    = fma(beta1, m, fma(-beta1, g, g))           lerp(g, m, beta1)
+ *   v    = fma(beta2, v, fma(-beta2, g*g, g*g))       lerp(g*g, v, beta2)
+ *   mh   = m / bc1;   vh = v / bc2
+ *   old  = master ? master[i] : (float)params[i]
+ *   wd_e = (tensor of i).decay ? weight_decay : 0
+ *   p    = old - lr * ( mh / (sqrt(vh) + eps) + wd_e * old )
+ *   master[i] = p                                      (if master != NULL)
+ *   params[i] = SR(p, global index of i, seed)
+ *
+ * SR(x, k, seed): x NaN -> 0x7FC0; otherwise b = bits(x),
+ *   params = (b >> 16) + ((b & 0xFFFF) > (noise(k, seed) & 0xFFFF) ? 1 : 0)
+ * i.e. the bf16 neighbour away from zero with probability (b & 0xFFFF)/65536,
+ * and noise() is the counter hash documented at mp_noise_u32.
+ *
+ *   params      bf16[n], device, read (no-master variant) and written.
+ *   grads       bf16[n], device, read only.
+ *   master      fp32[n], device, read and written; NULL selects the
+ *               no-master variant, which reads the old weight from params.
+ *   m, v        fp32[n], device, read and written.
+ *   global_offset, n   the covered global range; n == 0 is a no-op.
+ *   table, n_tensors   HOST array describing the whole flat buffer: sorted,
+ *               contiguous from offset 0, decay in {0,1}, reserved == 0, and
+ *               covering [global_offset, global_offset + n).
+ *   lr, beta1, beta2, eps, weight_decay   finite; beta1, beta2 in [0, 1).
+ *   d_grad_scale  float[1], device (normally mp_grad_norm's d_scale); NULL
+ *               means scale 1. If it holds NaN or Inf the kernel writes no
+ *               buffer at all and stores MP_ERR_NONFINITE into *d_status.
+ *   t           1-based step count (t >= 1).
+ *   seed        per-step rounding seed.
+ *   d_status    int32[1], device, may be NULL; written only on that device-
+ *               side error (the caller zeroes it and reads it after a sync).
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_TABLE, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
+                  float* m, float* v,
+                  uint64_t global_offset, uint64_t n,
+                  const mp_tensor_t* table, int32_t n_tensors,
+                  float lr, float beta1, float beta2, float eps,
+                  float weight_decay, const float* d_grad_scale,
+                  int32_t t, uint32_t seed, int32_t* d_status,
+                  void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Stochastic rounding fp32 -> bf16 of a range — [LLMC] §2.3 (the rounding
+ * rule) and §5.2 (rebuilding bf16 weights from the fp32 master with the
+ * saved rounding randomness).
+ *
+ *   out[i] = SR(in[i], global_offset + i, seed)  for i < n   (rule above)
+ *
+ *   out   bf16[n], device, written.   in   fp32[n], device, read only.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_stochastic_round(uint16_t* out, const float* in,
+                        uint64_t global_offset, uint64_t n, uint32_t seed,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The rounding randomness itself — [LLMC] §2.3 and §7 name SquirrelNoise5 /
+ * Get2dNoiseUint. noise(k, seed) is the 2D form of SquirrelNoise5 (Squirrel
+ * Eiserloh's published counter-based noise hash) at x = low 32 bits of k,
+ * y = high 32 bits of k:
+ *   pos = x + 198491317 * y (mod 2^32)
+ *   h = pos * 0xD2A80A3F;  h += seed;      h ^= h >> 9;
+ *   h += 0xA884F197;       h ^= h >> 11;
+ *   h *= 0x6C736F4B;       h ^= h >> 13;
+ *   h += 0xB79F3ABB;       h ^= h >> 15;
+ *   h *= 0x1B56C4F5;       h ^= h >> 17;      (all mod 2^32)
+ * It is keyed on the global element index, not on the launch geometry, so a
+ * result does not depend on grid shape or on how the buffer is sharded.
+ *
+ *   out[i] = noise(first_index + i, seed)   for i < n;  out uint32[n], device.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n,
+                 uint32_t seed, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MP_ADAMW_H */

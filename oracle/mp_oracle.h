@@ -1,0 +1,77 @@
+/*
+ * mp_oracle.h — plain, single-threaded CPU oracle of the mixed-precision
+ * AdamW + stochastic-rounding optimizer step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product (the CUDA library and its
+ * Python binding) may include, link, load or call this code; only the tests,
+ * the smoke check and the benchmark's CPU-baseline leg do. It shares no code,
+ * header, table or constant generator with the CUDA path: every function here
+ * is written from the pages' description of the method, cited per function.
+ *
+ * Sources (web pages, by title and section):
+ *   [LLMC]  llm.c code walk-through, ch. 04 "Multi-GPU and mixed precision":
+ *           §2.2 AdamW kernel, §2.3 stochastic rounding, §4 train step.
+ *   [CMU13] CMU 11-667 lecture 13 notes, "Scaling up LLMs: optimization and
+ *           parallel training": §1.7 bias correction and AdamW, §2.3 fp32
+ *           master weights, §7.3 exercises 1 and 5.
+ *
+ * Precision: the pages fix fp32 for the update (fp32 master, fp32 m/v, the
+ * bf16 grad converted to float before use), so the step is computed in fp32
+ * with one rounding per written operation and an explicit fmaf() for each of
+ * the two-FMA lerps; the gradient norm is a plain fp64 sum of squares.
+ * Compiled with -ffp-contract=off and without fast-math.
+ */
+#ifndef MP_ORACLE_H
+#define MP_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct oracle_tensor {
+    uint64_t offset; /* global element offset of the tensor */
+    uint64_t size;   /* element count                        */
+    int32_t decay;   /* 1: weight decay applies; 0: it does not */
+    int32_t pad;
+} oracle_tensor;
+
+/* SquirrelNoise5 (Squirrel Eiserloh), 2D form, at (low32(k), high32(k)). */
+uint32_t oracle_noise_u32(uint64_t k, uint32_t seed);
+void oracle_noise_fill(uint32_t* out, uint64_t first, uint64_t n, uint32_t seed);
+
+/* Stochastic rounding of one fp32 value with a given 16-bit random draw. */
+uint16_t oracle_sr_with_rand(float x, uint32_t rand16);
+/* Stochastic rounding keyed on (global index k, seed). */
+uint16_t oracle_sr(float x, uint64_t k, uint32_t seed);
+void oracle_stochastic_round(uint16_t* out, const float* in,
+                             uint64_t global_offset, uint64_t n, uint32_t seed);
+
+/* Gradient norm: plain fp64 sum of squares in index order, then sqrt. */
+double oracle_sumsq(const uint16_t* grads, uint64_t n);
+float oracle_clip_scale(float norm, float clip);
+void oracle_grad_norm(const uint16_t* grads, uint64_t n, float clip,
+                      double* sumsq, float* norm, float* scale);
+
+/* Bias-correction denominators 1 - beta^t for the 1-based step t. */
+void oracle_bias_corrections(float beta1, float beta2, int32_t t,
+                             float* bc1, float* bc2);
+
+/* One AdamW + SR step over [global_offset, global_offset + n) of the flat
+ * buffer described by `table`. master == NULL selects the no-master variant.
+ * Returns 0, or 5 (nothing written) if `scale` is not finite, or -1 if the
+ * table leaves part of the range uncovered. */
+int oracle_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
+                      float* m, float* v,
+                      uint64_t global_offset, uint64_t n,
+                      const oracle_tensor* table, int32_t n_tensors,
+                      float lr, float beta1, float beta2, float eps,
+                      float weight_decay, float scale,
+                      int32_t t, uint32_t seed);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,470 @@
+"""Pins of the CPU oracle to facts the pages and mathematics fix (no GPU).
+
+Each test checks the oracle against something other than itself: numbers the
+pages print (tests/golden/), closed forms of the first Adam step, invariants
+(no decay on 1D tensors, shard invariance), exhaustive enumeration of the
+rounding rule, a statistical check of unbiasedness, and library routines
+(torch.optim.AdamW in fp64, math.fsum, torch's bf16 cast).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+F32 = np.float32
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def bf16_value(bits):
+    return float(oracle.bf16_bits_to_f32(np.array([bits], dtype=np.uint16))[0])
+
+
+# --------------------------------------------------------------------------
+# Bias correction — CMU 11-667 lecture 13 notes §1.7 and §7.3 exercise 1.
+# --------------------------------------------------------------------------
+def test_bias_correction_multipliers_match_printed_values(golden):
+    rows = golden("bias_correction_multipliers.txt")
+    assert len(rows) == 11
+    for b1, b2, t, printed in rows:
+        bc1, bc2 = oracle.bias_corrections(float(b1), float(b2), int(t))
+        mult = float(bc1) / math.sqrt(float(bc2))
+        # printed to 3 significant figures: within half a unit of the last digit
+        digits = len(printed.split(".")[1])
+        assert abs(mult - float(printed)) <= 0.5 * 10 ** -digits + 1e-9, (b1, b2, t, mult, printed)
+
+
+def test_bias_correction_is_one_minus_beta_to_the_t():
+    # t = 1: bc = 1 - beta exactly as rounded once to float
+    bc1, bc2 = oracle.bias_corrections(0.9, 0.95, 1)
+    assert bc1 == F32(1.0 - float(F32(0.9))) and bc2 == F32(1.0 - float(F32(0.95)))
+    # large t: corrections tend to 1
+    bc1, bc2 = oracle.bias_corrections(0.9, 0.95, 10000)
+    assert bc1 == F32(1.0) and bc2 == F32(1.0)
+
+
+# --------------------------------------------------------------------------
+# First Adam step in closed form — llm.c ch. 04 §2.2 with m = v = 0, t = 1:
+# m = (1-b1) g, v = (1-b2) g^2, so m_hat = g, v_hat = g^2 and
+# p = old - lr * (g / (|g| + eps) + wd * old).
+# --------------------------------------------------------------------------
+def _one_tensor_step(g_vals, old, lr, b1, b2, eps, wd, decay=1, scale=1.0, t=1, master=True):
+    n = len(g_vals)
+    gbits = W.bf16_bits(torch.tensor(g_vals, dtype=torch.float32).to(torch.bfloat16))
+    g = oracle.bf16_bits_to_f32(gbits).astype(np.float64)
+    old = np.asarray(old, dtype=np.float32)
+    ms = old.copy()
+    params = W.bf16_bits(torch.from_numpy(old.copy()).to(torch.bfloat16)).copy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    st = oracle.adamw_step(params, gbits.copy(), ms if master else None, m, v, 0, [(0, n, decay)],
+                           lr, b1, b2, eps, wd, scale, t, 7)
+    assert st == 0
+    return g, old.astype(np.float64), ms, m, v, params
+
+
+@pytest.mark.parametrize("lr,wd,eps", [(1e-3, 0.1, 1e-8), (0.1, 0.5, 1e-8), (0.05, 0.0, 1e-3)])
+def test_first_step_closed_form(lr, wd, eps):
+    rng = np.random.default_rng(0)
+    n = 4096
+    g_vals = rng.standard_normal(n) * 10.0 ** rng.uniform(-6, 1, n)
+    old = (rng.standard_normal(n) * 0.05).astype(np.float32)
+    b1, b2 = 0.9, 0.95
+    g, old64, p, m, v, _ = _one_tensor_step(g_vals, old, lr, b1, b2, eps, wd)
+    B1, B2, LR, WD, EPS = (f32(x) for x in (b1, b2, lr, wd, eps))
+    # moments
+    np.testing.assert_allclose(m, (1.0 - B1) * g, rtol=2 ** -22, atol=0)
+    np.testing.assert_allclose(v, (1.0 - B2) * g * g, rtol=2 ** -21, atol=0)
+    # update: bias correction cancels (1 - beta) exactly up to rounding
+    expect = old64 - LR * (g / (np.abs(g) + EPS) + WD * old64)
+    err = np.abs(p.astype(np.float64) - expect)
+    bound = 2 ** -22 * (np.abs(old64) + LR * (1.0 + WD * np.abs(old64))) + 2 ** -24 * np.abs(expect)
+    assert (err <= bound).all(), float((err / bound).max())
+
+
+def test_first_step_moves_each_weight_by_lr_sign_g_when_eps_is_tiny():
+    rng = np.random.default_rng(1)
+    n = 2048
+    g_vals = rng.standard_normal(n) * 10.0 ** rng.uniform(-8, 2, n)
+    old = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    lr = 1e-3
+    g, old64, p, _, _, _ = _one_tensor_step(g_vals, old, lr, 0.9, 0.999, 1e-30, 0.0)
+    step = p.astype(np.float64) - old64
+    np.testing.assert_allclose(step, -f32(lr) * np.sign(g), rtol=1e-5, atol=2 ** -24 * 0.1)
+
+
+def test_no_master_variant_reads_old_weight_from_bf16():
+    rng = np.random.default_rng(2)
+    n = 512
+    g_vals = rng.standard_normal(n) * 1e-3
+    old = W.bf16_bits(torch.from_numpy((rng.standard_normal(n) * 0.05).astype(np.float32)).to(torch.bfloat16))
+    old_f = oracle.bf16_bits_to_f32(old)
+    g, old64, _, _, _, params = _one_tensor_step(g_vals, old_f, 0.01, 0.9, 0.95, 1e-8, 0.1, master=False)
+    expect = old64 - f32(0.01) * (g / (np.abs(g) + f32(1e-8)) + f32(0.1) * old64)
+    got = oracle.bf16_bits_to_f32(params).astype(np.float64)
+    # the bf16 result is one of the two bf16 neighbours of the fp32 update,
+    # which itself carries fp32 rounding of order 2^-23 (|old| + lr)
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(expect))) - 7)
+    fp32_err = 2 ** -22 * (np.abs(old64) + f32(0.01) * (1 + f32(0.1) * np.abs(old64)))
+    assert (np.abs(got - expect) <= ulp * 1.0001 + fp32_err).all()
+
+
+def test_nonfinite_scale_writes_nothing():
+    n = 64
+    params = np.arange(n, dtype=np.uint16)
+    grads = np.full(n, 0x3F80, dtype=np.uint16)
+    master = np.ones(n, np.float32)
+    m = np.ones(n, np.float32)
+    v = np.ones(n, np.float32)
+    for bad in (float("nan"), float("inf"), float("-inf")):
+        before = [a.copy() for a in (params, master, m, v)]
+        st = oracle.adamw_step(params, grads, master, m, v, 0, [(0, n, 1)],
+                               1e-3, 0.9, 0.95, 1e-8, 0.1, bad, 1, 3)
+        assert st == 5
+        for a, b in zip((params, master, m, v), before):
+            assert np.array_equal(a, b)
+
+
+# --------------------------------------------------------------------------
+# Decay only on 2D tensors — llm.c ch. 04 §2.2.
+# --------------------------------------------------------------------------
+def test_zero_gradient_leaves_1d_tensors_unchanged_and_decays_2d():
+    entries = W.layout(W.specs_for("tiny"))
+    tab = W.table(entries)
+    st = W.make_state("tiny")
+    master = st["master"].numpy().copy()
+    params = W.bf16_bits(st["params"]).copy()
+    N = master.size
+    m = np.zeros(N, np.float32)
+    v = np.zeros(N, np.float32)
+    grads = np.zeros(N, np.uint16)
+    lr, wd = 1e-3, 0.1
+    master0, params0 = master.copy(), params.copy()
+    assert oracle.adamw_step(params, grads, master, m, v, 0, tab, lr, 0.9, 0.95, 1e-8, wd, 1.0, 1, 11) == 0
+    LR, WD = F32(lr), F32(wd)
+    for e in entries:
+        sl = slice(e.offset, e.offset + e.size)
+        if e.spec.decay:
+            expect = master0[sl] - LR * (WD * master0[sl])  # fp32 ops, same rounding
+            assert np.array_equal(master[sl], expect), e.spec.name
+        else:
+            assert np.array_equal(master[sl], master0[sl]), e.spec.name
+            assert np.array_equal(params[sl], params0[sl]), e.spec.name  # 1 and 0 are exact in bf16
+    assert np.all(m == 0) and np.all(v == 0)
+
+
+# --------------------------------------------------------------------------
+# 16 steps against torch.optim.AdamW (fp64) on the 28,672-param model —
+# CMU 11-667 lecture 13 notes §1.6 check their optimizers against torch.optim
+# over 16 steps; llm.c's update is the same mathematics (decoupled decay).
+# --------------------------------------------------------------------------
+def test_sixteen_steps_track_torch_adamw_fp64():
+    name = "tiny"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    st = W.make_state(name)
+    master = st["master"].numpy().copy()
+    params = W.bf16_bits(st["params"]).copy()
+    N = master.size
+    m = np.zeros(N, np.float32)
+    v = np.zeros(N, np.float32)
+    H = {k: f32(x) for k, x in W.HYPER.items()}
+
+    ref = [torch.nn.Parameter(st["master"][e.offset:e.offset + e.size].double().clone()) for e in entries]
+    groups = [dict(params=[p for p, e in zip(ref, entries) if e.spec.decay], weight_decay=H["weight_decay"]),
+              dict(params=[p for p, e in zip(ref, entries) if not e.spec.decay], weight_decay=0.0)]
+    opt = torch.optim.AdamW(groups, lr=H["lr"], betas=(H["beta1"], H["beta2"]), eps=H["eps"], foreach=False)
+
+    scales = []
+    gmax = np.zeros(N)
+    for t in range(1, 17):
+        g = W.make_grads(name, t)
+        gbits = W.bf16_bits(g).copy()
+        _, norm, scale = oracle.grad_norm(gbits, H["clip"])
+        scales.append(float(scale))
+        assert oracle.adamw_step(params, gbits, master, m, v, 0, tab, H["lr"], H["beta1"], H["beta2"],
+                                 H["eps"], H["weight_decay"], float(scale), t, W.step_seed(t)) == 0
+        gd = g.double() * float(scale)
+        gmax = np.maximum(gmax, np.abs(gd.numpy()))
+        for p, e in zip(ref, entries):
+            p.grad = gd[e.offset:e.offset + e.size].clone()
+        opt.step()
+    assert max(scales) < 1.0  # clipping was active on every step
+    refp = torch.cat([p.detach() for p in ref]).numpy()
+    st_m = torch.cat([opt.state[p]["exp_avg"] for p in ref]).numpy()
+    st_v = torch.cat([opt.state[p]["exp_avg_sq"] for p in ref]).numpy()
+    # fp32 rounding: about one ulp per step of the largest magnitude the weight
+    # passed through, |p| <= |p0| + 16 lr (1 + wd |p|), over 16 steps
+    err = np.abs(master.astype(np.float64) - refp)
+    p0 = np.abs(st["master"].numpy().astype(np.float64))
+    bound = 16 * 2 ** -23 * (np.maximum(p0, np.abs(refp)) + 16 * H["lr"] * 1.2)
+    assert (err <= bound).all(), float((err / bound).max())
+    assert float(err.mean()) < 1e-8
+    # m is a signed average: its rounding error scales with the gradients it
+    # averaged, not with |m| (which may cross zero)
+    assert (np.abs(m - st_m) <= 16 * 2 ** -23 * (np.abs(st_m) + gmax)).all()
+    np.testing.assert_allclose(v, st_v, rtol=2e-6, atol=1e-16)
+    # the bf16 weights are a stochastic rounding of the fp32 master
+    pf = oracle.bf16_bits_to_f32(params).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(master.astype(np.float64)), 1e-30))) - 7)
+    assert (np.abs(pf - master) <= ulp).all()
+
+
+# --------------------------------------------------------------------------
+# Stochastic rounding — llm.c ch. 04 §2.3.
+# --------------------------------------------------------------------------
+SR_VALUES = [1.0 + 2 ** -9, -(1.0 + 3 * 2 ** -10), 257.0, 0.1, -3.3e-5, 1e-40, -2.5e-39, 3.0e38]
+
+
+def _bits(x):
+    return int(np.array([x], np.float32).view(np.uint32)[0])
+
+
+@pytest.mark.parametrize("x", SR_VALUES)
+def test_sr_exhaustive_over_all_draws(x):
+    b = _bits(x)
+    lo, trunc = b & 0xFFFF, b >> 16
+    ups = 0
+    for r in range(65536):
+        out = oracle.sr_with_rand(x, r)
+        assert out in (trunc, trunc + 1)
+        ups += out == trunc + 1
+    assert ups == lo  # P(away from zero) = lo16 / 65536 exactly
+    down = bf16_value(trunc)
+    up = bf16_value(trunc + 1)
+    xf = float(np.float32(x))
+    # truncation moves toward zero, the increment away from zero
+    assert abs(down) <= abs(xf) < abs(up) and math.copysign(1, down) == math.copysign(1, xf)
+    # {down, up} are x's two bf16 neighbours: torch's round-to-nearest cast picks one of them
+    assert torch.tensor(xf, dtype=torch.float64).to(torch.bfloat16).item() in (down, up)
+
+
+def test_sr_leaves_bf16_representable_values_unchanged():
+    rng = np.random.default_rng(3)
+    pats = rng.integers(0, 0x7F80, 4000).astype(np.uint32)
+    pats |= (rng.integers(0, 2, 4000).astype(np.uint32) << 15)
+    xs = (pats << 16).view(np.float32)
+    for x, p in zip(xs[:400], pats[:400]):
+        for r in (0, 1, 0x7FFF, 0xFFFF):
+            assert oracle.sr_with_rand(float(x), r) == p
+    out = oracle.stochastic_round(xs, 12345, 99)
+    assert np.array_equal(out, pats.astype(np.uint16))
+
+
+def test_sr_special_values():
+    assert oracle.sr_with_rand(float("inf"), 0) == 0x7F80
+    assert oracle.sr_with_rand(float("-inf"), 0) == 0xFF80
+    assert oracle.sr_with_rand(0.0, 0) == 0x0000
+    assert oracle.sr_with_rand(-0.0, 0) == 0x8000
+    assert oracle.sr_with_rand(float("nan"), 0xFFFF) == 0x7FC0
+    nan_low = np.array([0x7F800001], np.uint32).view(np.float32)[0]
+    assert oracle.sr_with_rand(float(nan_low), 0xFFFF) == 0x7FC0
+    # the largest finite fp32 rounds to bf16 max or to +Inf (carry into the exponent)
+    big = float(np.finfo(np.float32).max)
+    assert oracle.sr_with_rand(big, 0xFFFF) == 0x7F7F
+    assert oracle.sr_with_rand(big, 0) == 0x7F80
+    # smallest subnormal: up w.p. 1/65536 ... to the smallest bf16 subnormal
+    tiny = float(np.array([1], np.uint32).view(np.float32)[0])
+    assert oracle.sr_with_rand(tiny, 0) == 0x0001
+    assert oracle.sr_with_rand(tiny, 1) == 0x0000
+
+
+@pytest.mark.parametrize("x", [1.0 + 2 ** -9, -0.3, 7.77e-3, 1.0 + 2 ** -8])
+def test_sr_is_unbiased_over_1e5_seeds(x):
+    """The mean over 10^5 seeds lies within 4 sigma of x (llm.c ch. 04 §2.3:
+    the rounding equals the true value in expectation)."""
+    L = oracle.lib()
+    n = 100_000
+    k = 987654321
+    outs = np.fromiter((L.oracle_sr(x, k, s) for s in range(n)), dtype=np.uint16, count=n)
+    vals = oracle.bf16_bits_to_f32(outs).astype(np.float64)
+    b = _bits(x)
+    f = (b & 0xFFFF) / 65536.0
+    ulp = abs(bf16_value((b >> 16) + 1) - bf16_value(b >> 16))
+    sigma = ulp * math.sqrt(f * (1 - f)) / math.sqrt(n)
+    xf = float(np.float32(x))
+    assert abs(vals.mean() - xf) <= 4 * sigma, (vals.mean() - xf, sigma)
+
+
+def test_sr_halfway_values_from_bf16_facts(golden):
+    """257 and 1 + 2^-8 sit exactly half-way between two bf16 values (CMU
+    11-667 lecture 13 notes §7.3 exercise 5); SR sends exactly half of all
+    draws each way, where round-to-nearest-even always picks the even one."""
+    for x, lo_val, hi_val in ((257.0, 256.0, 258.0), (1.0 + 2 ** -8, 1.0, 1.0078125)):
+        outs = [bf16_value(oracle.sr_with_rand(x, r)) for r in range(65536)]
+        assert outs.count(hi_val) == 32768 and outs.count(lo_val) == 32768
+
+
+def test_bf16_facts_of_the_input_cast(golden):
+    for fmt, x, expect in golden("bf16_facts.txt"):
+        dt = torch.bfloat16 if fmt == "bf16" else torch.float16
+        got = torch.tensor(float(x), dtype=torch.float64).to(dt).double().item()
+        assert got == float(expect), (fmt, x, got)
+
+
+# --------------------------------------------------------------------------
+# Rounding randomness: uniform low 16 bits (what makes SR unbiased).
+# Its exact values follow the published SquirrelNoise5 definition; the pages
+# print no test vector for it.
+# --------------------------------------------------------------------------
+def _chi2_uniform16(vals):
+    counts = np.bincount(vals.astype(np.int64), minlength=65536)
+    e = vals.size / 65536.0
+    return float(((counts - e) ** 2 / e).sum())
+
+
+@pytest.mark.parametrize("first,seed", [(0, 0), (123456789, 42), ((1 << 32) - 100000, 7), (5 << 32, 2024)])
+def test_noise_low16_uniform_chi2(first, seed):
+    r = oracle.noise_fill(first, 1 << 22, seed)
+    chi2 = _chi2_uniform16(r & 0xFFFF)
+    dof = 65535
+    assert abs(chi2 - dof) < 6 * math.sqrt(2 * dof), chi2
+    chi2_hi = _chi2_uniform16(r >> 16)
+    assert abs(chi2_hi - dof) < 6 * math.sqrt(2 * dof), chi2_hi
+
+
+def test_noise_over_seeds_uniform_and_uncorrelated():
+    L = oracle.lib()
+    n = 1 << 20
+    r = np.fromiter((L.oracle_noise_u32(77, s) for s in range(n)), dtype=np.uint32, count=n)
+    chi2 = _chi2_uniform16(r & 0xFFFF)
+    assert abs(chi2 - 65535) < 6 * math.sqrt(2 * 65535)
+    a = oracle.noise_fill(1000, n + 1, 5).astype(np.float64)
+    for x, y in ((a[:-1], a[1:]), (r[:-1].astype(np.float64), r[1:].astype(np.float64))):
+        c = np.corrcoef(x, y)[0, 1]
+        assert abs(c) < 5 / math.sqrt(n), c
+    b = oracle.noise_fill(1000, n, 6).astype(np.float64)
+    assert abs(np.corrcoef(a[:-1], b)[0, 1]) < 5 / math.sqrt(n)
+
+
+def test_noise_depends_on_the_high_index_word():
+    lo = oracle.noise_fill(0, 4096, 9)
+    hi = oracle.noise_fill(1 << 32, 4096, 9)
+    assert np.mean(lo == hi) < 0.01
+
+
+# --------------------------------------------------------------------------
+# Gradient norm and clip scale — llm.c ch. 04 §4.
+# --------------------------------------------------------------------------
+def test_norm_of_all_ones_is_sqrt_n():
+    for n in (1, 7, 28672, 1 << 20):
+        s, nrm, sc = oracle.grad_norm(np.full(n, 0x3F80, np.uint16), 1.0)
+        assert s == float(n)
+        assert nrm == F32(math.sqrt(n))
+        assert sc == (F32(1.0) / F32(math.sqrt(n)) if n > 1 else F32(1.0))
+
+
+def test_norm_of_power_of_two_pattern_is_exact():
+    n = 100003
+    k = np.arange(n) % 9 - 4
+    vals = np.ldexp(1.0, k) * np.where(np.arange(n) % 2 == 0, 1.0, -1.0)
+    bits = W.bf16_bits(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16))
+    s = oracle.sumsq(bits)
+    assert s == float(sum(4.0 ** int(e) for e in k))  # every partial sum is exact
+
+
+def test_norm_matches_math_fsum():
+    rng = np.random.default_rng(4)
+    for n, scale in ((1000, 1e-3), (200003, 1.0), (50000, 1e20), (5000, 1e-25)):
+        vals = rng.standard_normal(n) * scale
+        bits = W.bf16_bits(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16))
+        g = oracle.bf16_bits_to_f32(bits).astype(np.float64)
+        exact = math.fsum(g * g)  # squares of bf16 values are exact in fp64
+        s = oracle.sumsq(bits)
+        assert abs(s - exact) <= n * 2 ** -53 * exact
+
+
+def test_clip_scale_rule():
+    cs = oracle.clip_scale
+    assert cs(2.0, 1.0) == F32(0.5)
+    assert cs(0.5, 1.0) == F32(1.0)
+    assert cs(1.0, 1.0) == F32(1.0)
+    assert cs(0.0, 1.0) == F32(1.0)
+    assert cs(3.0, 1.0) == F32(1.0) / F32(3.0)
+    assert cs(10.0, 2.5) == F32(0.25)
+    for bad in (float("nan"), float("inf")):
+        assert math.isnan(cs(bad, 1.0))
+
+
+def test_norm_with_nonfinite_grads_gives_nan_scale():
+    g = np.full(100, 0x3F80, np.uint16)
+    g[37] = 0x7FC0
+    _, nrm, sc = oracle.grad_norm(g, 1.0)
+    assert math.isnan(nrm) and math.isnan(sc)
+    g[37] = 0xFF80  # -inf
+    _, nrm, sc = oracle.grad_norm(g, 1.0)
+    assert math.isinf(nrm) and math.isnan(sc)
+
+
+# --------------------------------------------------------------------------
+# ZeRO-1 shards — CMU 11-667 lecture 13 notes §5.2 (max difference 0 versus
+# data parallelism); llm.c ch. 04 §3.2 (contiguous num_params / world slices).
+# --------------------------------------------------------------------------
+def test_shard_bytes_of_the_tiny_model(golden):
+    kv = {k: int(v) for k, v in golden("zero1_state_bytes.txt")}
+    N = W.total(W.layout(W.specs_for("tiny")))
+    assert N == kv["params"]
+    assert 8 * N == kv["adam_state_bytes_full"]
+    assert 8 * N // kv["cards"] == kv["adam_state_bytes_per_card"]
+
+
+@pytest.mark.parametrize("with_master", [True, False])
+def test_sharded_steps_equal_whole_buffer_steps(with_master):
+    name = "tiny"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    st = W.make_state(name)
+    N = W.total(entries)
+    whole = dict(params=W.bf16_bits(st["params"]).copy(), master=st["master"].numpy().copy(),
+                 m=np.zeros(N, np.float32), v=np.zeros(N, np.float32))
+    shard = {k: a.copy() for k, a in whole.items()}
+    H = W.HYPER
+    world = 4
+    for t in range(1, 41):
+        g = W.bf16_bits(W.make_grads(name, t)).copy()
+        _, _, scale = oracle.grad_norm(g, H["clip"])
+        args = (H["lr"], H["beta1"], H["beta2"], H["eps"], H["weight_decay"], float(scale), t, W.step_seed(t))
+        oracle.adamw_step(whole["params"], g, whole["master"] if with_master else None, whole["m"], whole["v"],
+                          0, tab, *args)
+        per = N // world
+        for r in range(world):
+            sl = slice(r * per, (r + 1) * per)
+            views = {k: shard[k][sl] for k in shard}
+            assert oracle.adamw_step(views["params"], g[sl].copy(), views["master"] if with_master else None,
+                                     views["m"], views["v"], r * per, tab, *args) == 0
+    for k in whole:
+        if k == "master" and not with_master:
+            continue
+        assert np.array_equal(whole[k], shard[k]), k
+
+
+# --------------------------------------------------------------------------
+# Why stochastic rounding: small updates survive (llm.c ch. 04 §2.3; CMU
+# 11-667 lecture 13 notes §2.3). Constant update 1e-4 |w0| for 1000 steps.
+# --------------------------------------------------------------------------
+def test_sr_tracks_small_updates_where_round_to_nearest_stalls():
+    n = 1 << 14
+    w0 = W.sr_stress_weights(n).numpy()
+    delta = (np.float32(1e-4) * np.abs(w0)).astype(np.float32)
+    fp32 = w0.copy()
+    sr_bits = W.bf16_bits(torch.from_numpy(w0).to(torch.bfloat16)).copy()
+    rne = torch.from_numpy(w0).to(torch.bfloat16)
+    for t in range(1, 1001):
+        fp32 = (fp32 + delta).astype(np.float32)
+        x = (oracle.bf16_bits_to_f32(sr_bits) + delta).astype(np.float32)
+        sr_bits = oracle.stochastic_round(x, 0, W.step_seed(t))
+        rne = (rne.float() + torch.from_numpy(delta)).to(torch.bfloat16)
+    rel_rne = float(np.mean(rne.float().numpy().astype(np.float64) / fp32 - 1.0))
+    rel_sr = float(np.mean(oracle.bf16_bits_to_f32(sr_bits).astype(np.float64) / fp32 - 1.0))
+    # round-to-nearest never moves (the update is below half a bf16 step):
+    assert np.array_equal(rne.float().numpy(), torch.from_numpy(w0).to(torch.bfloat16).float().numpy())
+    # so its relative drift is w0 / (w0 + 1000 * 1e-4 |w0|) - 1 = -1/11 for w0 > 0 and +1/9 for w0 < 0
+    expect = float(np.mean(np.where(w0 > 0, 1 / 1.1 - 1, 1 / 0.9 - 1)))
+    assert abs(rel_rne - expect) < 2e-3
+    assert abs(rel_sr) < 2e-3  # SR follows the fp32 trajectory in expectation
