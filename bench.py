@@ -1,0 +1,473 @@
+"""Benchmark of the mixed-precision optimizer step on GB300.
+
+One step = the whole hot path over the GPT-2 124M parameter set (124,475,904
+params, 148 tensors, one flat buffer): global grad norm + clip scale
+(mp_grad_norm: two kernels) and the fused AdamW + stochastic-rounding step
+with fp32 master weights (mp_adamw_step: one kernel). Inputs are synthetic and
+already resident in HBM; the 3.5 GB of state touched per step is far larger
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0). Also reports: the roofline of the dominant
+kernel (the step kernel, 28 algorithmic bytes per parameter) against the
+measured HBM copy bandwidth, the other path variants (no-master step, norm,
+standalone rounding, 8 ZeRO-1 shard launches), an end-to-end number through
+the C ABI with the gradients copied from pinned host memory every step, SM
+clocks sampled during the timed region, and the CPU oracle timed on a bounded
+sample as a reported baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica of the step on its own GPU (weak scaling, no data-path collective);
+the time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "AdamW+SR step: Gparams/s and HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "Gparams/s"
+WORKLOAD = "gpt2_124m"
+STEP_BYTES_MASTER = 28   # 2 grad + 3x4 (master, m, v) read; 3x4 + 2 (param) written
+STEP_BYTES_NOMASTER = 22
+NORM_BYTES = 2
+SR_BYTES = 6
+FALLBACK_HBM_GBS = 6800.0
+STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
+                       "mixed_precision_adamw_gb300/csrc/mp_device.cuh"]
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (timing only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar (the step time) over all ranks."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(params_per_rank: int, world: int, steps: int, max_seconds: float) -> float:
+    """Gparams/s over all ranks: every rank updates params_per_rank per step."""
+    return params_per_rank * world * steps / max_seconds / 1e9
+
+
+# ---------------------------------------------------------------------------
+# measurement helpers
+# ---------------------------------------------------------------------------
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in STEP_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic_bytes():
+    """DRAM bytes per launch of the step kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        text = open(TRAFFIC_PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        if shutil.which("nvidia-smi") is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.fh = open(self.path, "w")
+        self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                                      "--format=csv,noheader,nounits", "-lms", "200"],
+                                     stdout=self.fh, stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import mixed_precision_adamw_gb300 as mp
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    H = W.HYPER
+    entries = W.layout(W.specs_for(WORKLOAD))
+    if args.params:
+        entries = prefix_entries(entries, args.params)
+    tab = W.table(entries)
+    N = W.total(entries)
+    st = W.make_state(WORKLOAD, device=device, entries=entries)
+    grads = [W.make_grads(WORKLOAD, s, device=device, entries=entries) for s in (1, 2)]
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"], device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
+    step_no = [0]
+
+    def one_step(ev_pair=None):
+        step_no[0] += 1
+        t = step_no[0]
+        g = grads[t % 2]
+        mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N, stream=stream)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        mp.mp_adamw_step(st["params"], g, st["master"], st["m"], st["v"], opt.table, d_grad_scale=opt.d_scale,
+                         t=t, seed=W.step_seed(t), d_status=opt.d_status, n=N, stream=stream, **kw)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(pairs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    step_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+    opt.check_status()
+    max_s = max_over_ranks(total_ms / 1e3, world, device)
+    value = whole_job_value(N, world, args.steps, max_s)
+    ms_per_step = max_s * 1e3 / args.steps
+
+    peak, peak_kind = measured_hbm_peak()
+    achieved = STEP_BYTES_MASTER * N / (step_kernel_ms / 1e3) / 1e9
+    traffic = profiled_traffic_bytes()
+    roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master>", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "traffic": traffic, "algorithmic_bytes_per_launch": STEP_BYTES_MASTER * N,
+                "kernel_ms": round(step_kernel_ms, 5)}
+
+    if args.quick:
+        variants, e2e = None, None
+    else:
+        variants = measure_variants(mp, st, grads[0], opt, N, entries, tab, stream, device, peak)
+        e2e = measure_e2e(mp, st, grads[0], opt, N, stream, device, kw, min(args.steps, 200), step_no)
+
+    if rank != 0:
+        return None
+    launches_per_step = 3  # norm partials + norm finalize + one step launch (<= 1024 decay segments)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
+                   "params": N, "tensors": len(entries), "variant": "fp32 master + bf16 params, clip 1.0",
+                   "bytes_per_param": STEP_BYTES_MASTER + NORM_BYTES,
+                   "l2": "no flush: 3.7 GB touched per step, > 129 MB L2",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "hbm_gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N * args.steps / (total_ms / 1e3) / 1e9, 1),
+        "hbm_frac_of_measured": round((STEP_BYTES_MASTER + NORM_BYTES) * N * args.steps / (total_ms / 1e3)
+                                      / 1e9 / peak, 4),
+        "roofline": roofline, "variants": variants, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if args.params:
+        line["config"]["workload"] += f", first {N} params only"
+        line["roofline"]["traffic"] = None
+    if world == 1 and not args.no_cpu_baseline and not args.quick:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+def time_events(fn, iters, stream):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    fn()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
+    H = W.HYPER
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
+    out = {}
+    iters = 20
+    ms = time_events(lambda: mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N,
+                                             stream=stream), iters, stream)
+    out["grad_norm"] = {"ms": round(ms, 5), "gbs": round(NORM_BYTES * N / ms / 1e6, 1),
+                        "frac": round(NORM_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_param": NORM_BYTES}
+    # no-master variant on its own state (params, m, v)
+    p2 = st["params"].clone()
+    m2 = st["m"].clone()
+    v2 = st["v"].clone()
+    ms = time_events(lambda: mp.mp_adamw_step(p2, g, None, m2, v2, opt.table, d_grad_scale=opt.d_scale, t=5,
+                                              seed=5, n=N, stream=stream, **kw), iters, stream)
+    out["step_no_master"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+                             "gbs": round(STEP_BYTES_NOMASTER * N / ms / 1e6, 1),
+                             "frac": round(STEP_BYTES_NOMASTER * N / ms / 1e6 / peak, 4),
+                             "bytes_per_param": STEP_BYTES_NOMASTER}
+    del p2, m2, v2
+    ms = time_events(lambda: mp.mp_stochastic_round(st["params"], st["master"], 7, n=N, stream=stream), iters,
+                     stream)
+    out["stochastic_round"] = {"ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
+                               "gbs": round(SR_BYTES * N / ms / 1e6, 1),
+                               "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
+    per = N // 8
+
+    def shards():
+        for r in range(8):
+            sl = slice(r * per, (r + 1) * per)
+            mp.mp_adamw_step(st["params"][sl], g[sl], st["master"][sl], st["m"][sl], st["v"][sl], opt.table,
+                             d_grad_scale=opt.d_scale, t=6, seed=6, global_offset=r * per, n=per, stream=stream,
+                             **kw)
+    ms = time_events(shards, iters // 2, stream)
+    out["step_8_shards"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+                            "gbs": round(STEP_BYTES_MASTER * N / ms / 1e6, 1), "launches": 8}
+    return out
+
+
+def measure_e2e(mp, st, g, opt, N, stream, device, kw, iters, step_no):
+    """Through the C ABI with host buffers: every step copies the bf16
+    gradients from pinned host memory and reads the norm and status back."""
+    H = W.HYPER
+    host_g = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
+    host_g.copy_(g.cpu())
+    dev_g = torch.empty_like(g)
+    host_out = torch.empty(2, dtype=torch.int32, pin_memory=True)
+
+    def step():
+        step_no[0] += 1
+        t = step_no[0]
+        dev_g.copy_(host_g, non_blocking=True)
+        mp.mp_grad_norm(dev_g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N, stream=stream)
+        mp.mp_adamw_step(st["params"], dev_g, st["master"], st["m"], st["v"], opt.table, d_grad_scale=opt.d_scale,
+                         t=t, seed=W.step_seed(t), d_status=opt.d_status, n=N, stream=stream, **kw)
+        host_out[0:1].copy_(opt.d_norm.view(torch.int32), non_blocking=True)
+        host_out[1:2].copy_(opt.d_status, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(iters):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": round(N * iters / (ms / 1e3) / 1e9, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * N,
+            "d2h_bytes_per_step": 8, "steps": iters, "ms_per_step": round(ms / iters, 5),
+            "h2d": "bf16 grads from pinned host memory, same stream"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline; reference arm)
+# ---------------------------------------------------------------------------
+def prefix_entries(entries, n):
+    out = []
+    for e in entries:
+        if e.offset >= n:
+            break
+        size = min(e.size, n - e.offset)
+        out.append(W.Entry(W.TensorSpec(e.spec.name, (size,) if len(e.spec.shape) == 1 else (1, size),
+                                        e.spec.kind), e.offset))
+    return out
+
+
+class OracleSample:
+    """The first `n` params of the workload on the host, stepped by the oracle."""
+
+    def __init__(self, n):
+        import oracle
+        self.oracle = oracle
+        entries = prefix_entries(W.layout(W.specs_for(WORKLOAD)), n)
+        self.tab = W.table(entries)
+        st = W.make_state(WORKLOAD, entries=entries)
+        self.params = W.bf16_bits(st["params"]).copy()
+        self.master = st["master"].numpy().copy()
+        self.m = st["m"].numpy().copy()
+        self.v = st["v"].numpy().copy()
+        self.grads = [W.bf16_bits(W.make_grads(WORKLOAD, s, entries=entries)).copy() for s in (1, 2)]
+        self.n = n
+        self.t = 0
+
+    def step(self):
+        H = W.HYPER
+        self.t += 1
+        g = self.grads[self.t % 2]
+        _, _, scale = self.oracle.grad_norm(g, H["clip"])
+        st = self.oracle.adamw_step(self.params, g, self.master, self.m, self.v, 0, self.tab, H["lr"], H["beta1"],
+                                    H["beta2"], H["eps"], H["weight_decay"], float(scale), self.t,
+                                    W.step_seed(self.t))
+        assert st == 0
+
+
+def cpu_baseline(seconds):
+    n = 1 << 22
+    s = OracleSample(n)
+    s.step()
+    t0 = time.perf_counter()
+    steps = 0
+    while time.perf_counter() - t0 < seconds:
+        s.step()
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {n} params of the GPT-2 124M set, {steps} steps (norm + AdamW + SR), "
+                      f"{dt:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    budget = args.cpu_seconds if args.cpu_seconds else 30.0
+    probe = OracleSample(1 << 18)
+    t0 = time.perf_counter()
+    probe.step()
+    per_param = (time.perf_counter() - t0) / probe.n
+    total_steps = args.steps + args.warmup
+    n = int(budget / max(1, total_steps) / per_param)
+    n = max(1 << 12, min(n, 1 << 24)) & ~7
+    s = OracleSample(n)
+    for _ in range(args.warmup):
+        s.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        s.step()
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt / 1e9
+    sample = f"first {n} params of the GPT-2 124M set per step (norm + AdamW + SR), single-threaded C oracle"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
+                       "params": W.total(W.layout(W.specs_for(WORKLOAD))), "sample_params_per_step": n},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--params", type=int, default=0,
+                    help="use only the first P params of the set (small cases for profiling)")
+    ap.add_argument("--quick", action="store_true",
+                    help="time the step only: no variants, end-to-end or CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

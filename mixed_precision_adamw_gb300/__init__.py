@@ -1,0 +1,234 @@
+"""mixed_precision_adamw_gb300 — Python binding of libmpadamw.so.
+
+A thin ctypes layer over the C ABI in include/mp_adamw.h: it checks tensor
+dtypes, devices and sizes, passes raw device pointers and the current CUDA
+stream, and raises MpError on a non-OK status. Every step of the optimizer
+runs in the library's CUDA kernels; there is no fallback of any kind, and
+importing this package fails if the compiled library is missing.
+
+PyTorch is used only for device memory and streams. bf16 arrays are passed
+as torch.bfloat16 (or int16/uint16) tensors holding the raw patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Iterable, Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmpadamw.so")
+
+MP_OK = 0
+MP_ERR_NULL = 1
+MP_ERR_ALIGN = 2
+MP_ERR_TABLE = 3
+MP_ERR_RANGE = 4
+MP_ERR_NONFINITE = 5
+MP_ERR_CUDA = 6
+MP_ERR_WORKSPACE = 7
+
+
+class MpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}"
+                         + (f" (cudaError {last_cuda_error()})" if status == MP_ERR_CUDA else ""))
+
+
+class MpTensor(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_uint64), ("size", ctypes.c_uint64),
+                ("decay", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -m mixed_precision_adamw_gb300.build` "
+            "(nvcc, sm_103a). There is no fallback path.")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, u64, u32, i32, f32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_float
+    L.mp_abi_version.restype = ctypes.c_int
+    L.mp_abi_version.argtypes = []
+    L.mp_status_string.restype = ctypes.c_char_p
+    L.mp_status_string.argtypes = [ctypes.c_int]
+    L.mp_last_cuda_error.restype = ctypes.c_int
+    L.mp_last_cuda_error.argtypes = []
+    L.mp_grad_norm_workspace_bytes.restype = ctypes.c_size_t
+    L.mp_grad_norm_workspace_bytes.argtypes = [u64]
+    L.mp_grad_norm.restype = ctypes.c_int
+    L.mp_grad_norm.argtypes = [vp, u64, f32, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    L.mp_adamw_step.restype = ctypes.c_int
+    L.mp_adamw_step.argtypes = [vp, vp, vp, vp, vp, u64, u64, ctypes.POINTER(MpTensor), i32,
+                                f32, f32, f32, f32, f32, vp, i32, u32, vp, vp]
+    L.mp_stochastic_round.restype = ctypes.c_int
+    L.mp_stochastic_round.argtypes = [vp, vp, u64, u64, u32, vp]
+    L.mp_noise_u32.restype = ctypes.c_int
+    L.mp_noise_u32.argtypes = [vp, u64, u64, u32, vp]
+    return L
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def abi_version() -> int:
+    return int(_lib.mp_abi_version())
+
+
+def status_string(status: int) -> str:
+    return _lib.mp_status_string(status).decode()
+
+
+def last_cuda_error() -> int:
+    return int(_lib.mp_last_cuda_error())
+
+
+def _check(status: int, what: str):
+    if status != MP_OK:
+        raise MpError(status, what)
+
+
+_BF16_LIKE = (torch.bfloat16, torch.int16, torch.uint16)
+
+
+def _ptr(t: Optional[torch.Tensor], dtypes, name: str, n: Optional[int] = None) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name}: {t.numel()} elements < {n}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+class TensorTable:
+    """The flat parameter buffer's tensor table, packed once for reuse.
+
+    entries: iterable of (offset, size, decay) with global element offsets.
+    """
+
+    def __init__(self, entries: Iterable[Tuple[int, int, int]]):
+        entries = list(entries)
+        self.n_tensors = len(entries)
+        self._arr = (MpTensor * max(1, self.n_tensors))()
+        for i, (off, size, decay) in enumerate(entries):
+            self._arr[i].offset = int(off)
+            self._arr[i].size = int(size)
+            self._arr[i].decay = int(decay)
+            self._arr[i].reserved = 0
+        self.total = (entries[-1][0] + entries[-1][1]) if entries else 0
+
+    @property
+    def ctypes_array(self):
+        return self._arr
+
+
+def mp_grad_norm_workspace_bytes(n: int) -> int:
+    return int(_lib.mp_grad_norm_workspace_bytes(n))
+
+
+def mp_grad_norm(grads: torch.Tensor, clip: float, workspace: torch.Tensor, d_norm: torch.Tensor,
+                 d_scale: torch.Tensor, d_sumsq: Optional[torch.Tensor] = None, n: Optional[int] = None,
+                 stream=None) -> None:
+    """Enqueue the global gradient norm and clip scale (device outputs)."""
+    n = grads.numel() if n is None else n
+    st = _lib.mp_grad_norm(
+        _ptr(grads, _BF16_LIKE, "grads", n), n, clip,
+        _ptr(workspace, (torch.uint8, torch.float64, torch.int64), "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _ptr(d_norm, (torch.float32,), "d_norm", 1), _ptr(d_scale, (torch.float32,), "d_scale", 1),
+        _ptr(d_sumsq, (torch.float64,), "d_sumsq", 1), _stream(stream))
+    _check(st, "mp_grad_norm")
+
+
+def mp_adamw_step(params: torch.Tensor, grads: torch.Tensor, master: Optional[torch.Tensor],
+                  m: torch.Tensor, v: torch.Tensor, table: TensorTable, *, lr: float, beta1: float,
+                  beta2: float, eps: float, weight_decay: float, d_grad_scale: Optional[torch.Tensor],
+                  t: int, seed: int, global_offset: int = 0, n: Optional[int] = None,
+                  d_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Enqueue one AdamW + stochastic-rounding step over [global_offset, global_offset + n)."""
+    n = m.numel() if n is None else n
+    st = _lib.mp_adamw_step(
+        _ptr(params, _BF16_LIKE, "params", n), _ptr(grads, _BF16_LIKE, "grads", n),
+        _ptr(master, (torch.float32,), "master", n), _ptr(m, (torch.float32,), "m", n),
+        _ptr(v, (torch.float32,), "v", n), global_offset, n, table.ctypes_array, table.n_tensors,
+        lr, beta1, beta2, eps, weight_decay, _ptr(d_grad_scale, (torch.float32,), "d_grad_scale", 1),
+        t, seed & 0xFFFFFFFF, _ptr(d_status, (torch.int32,), "d_status", 1), _stream(stream))
+    _check(st, "mp_adamw_step")
+
+
+def mp_stochastic_round(out: torch.Tensor, inp: torch.Tensor, seed: int, global_offset: int = 0,
+                        n: Optional[int] = None, stream=None) -> None:
+    """Enqueue out[i] = SR(inp[i], global_offset + i, seed)."""
+    n = inp.numel() if n is None else n
+    st = _lib.mp_stochastic_round(_ptr(out, _BF16_LIKE, "out", n), _ptr(inp, (torch.float32,), "in", n),
+                                  global_offset, n, seed & 0xFFFFFFFF, _stream(stream))
+    _check(st, "mp_stochastic_round")
+
+
+def mp_noise_u32(out: torch.Tensor, first_index: int, seed: int, n: Optional[int] = None, stream=None) -> None:
+    """Enqueue out[i] = noise(first_index + i, seed) (the rounding draws)."""
+    n = out.numel() if n is None else n
+    st = _lib.mp_noise_u32(_ptr(out, (torch.int32, torch.uint32), "out", n), first_index, n,
+                           seed & 0xFFFFFFFF, _stream(stream))
+    _check(st, "mp_noise_u32")
+
+
+class Optimizer:
+    """Convenience wrapper holding the device state of one optimizer step:
+    workspace, norm/scale/status scalars and the packed tensor table.
+
+    step() enqueues mp_grad_norm then mp_adamw_step on the current stream and
+    does not synchronise; call check_status() after a sync to learn whether a
+    step was refused for a non-finite norm.
+    """
+
+    def __init__(self, table_entries: Sequence[Tuple[int, int, int]], *, lr: float, beta1: float,
+                 beta2: float, eps: float, weight_decay: float, clip: float, device=None):
+        self.table = TensorTable(table_entries)
+        self.n = self.table.total
+        self.hyper = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
+        self.clip = clip
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        nbytes = mp_grad_norm_workspace_bytes(self.n)
+        self.workspace = torch.empty(max(8, nbytes), dtype=torch.uint8, device=dev)
+        self.d_norm = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.d_scale = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.d_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(self, params, grads, master, m, v, t: int, seed: int, stream=None):
+        mp_grad_norm(grads, self.clip, self.workspace, self.d_norm, self.d_scale, n=self.n, stream=stream)
+        mp_adamw_step(params, grads, master, m, v, self.table, d_grad_scale=self.d_scale, t=t, seed=seed,
+                      d_status=self.d_status, n=self.n, stream=stream, **self.hyper)
+
+    def check_status(self) -> None:
+        st = int(self.d_status.item())
+        if st != MP_OK:
+            self.d_status.zero_()
+            raise MpError(st, "mp_adamw_step (device)")
+
+
+__all__ = [
+    "MpError", "MpTensor", "TensorTable", "Optimizer", "lib", "abi_version", "status_string",
+    "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_adamw_step",
+    "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",
+]

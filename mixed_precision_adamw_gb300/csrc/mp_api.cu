@@ -1,0 +1,221 @@
+// mp_api.cu — the C ABI declared in include/mp_adamw.h: argument checks,
+// host-side scalars (bias corrections, decay segments) and kernel launches.
+// Nothing here synchronises, allocates device memory, prints or exits.
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "mp_adamw.h"
+#include "mp_internal.h"
+
+namespace {
+
+constexpr uint64_t kMaxN = 1ull << 62;
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return MP_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+namespace mpk {
+
+cudaError_t device_info(DeviceInfo* out) {
+  static int sms_cache[64];  // 0 = not yet queried
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+  }
+  out->device = dev;
+  out->sms = sms;
+  return cudaSuccess;
+}
+
+}  // namespace mpk
+
+extern "C" {
+
+int mp_abi_version(void) { return MP_ABI_VERSION; }
+
+const char* mp_status_string(int status) {
+  switch (status) {
+    case MP_OK: return "MP_OK";
+    case MP_ERR_NULL: return "MP_ERR_NULL: a required pointer is NULL";
+    case MP_ERR_ALIGN: return "MP_ERR_ALIGN: a pointer is not aligned to its element size";
+    case MP_ERR_TABLE: return "MP_ERR_TABLE: tensor table malformed or not covering the range";
+    case MP_ERR_RANGE: return "MP_ERR_RANGE: a size, step or hyperparameter is out of range";
+    case MP_ERR_NONFINITE: return "MP_ERR_NONFINITE: the clip scale was NaN or Inf; nothing was written";
+    case MP_ERR_CUDA: return "MP_ERR_CUDA: a CUDA runtime call failed";
+    case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown mp_status";
+  }
+}
+
+int mp_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t mp_grad_norm_workspace_bytes(uint64_t n) {
+  mpk::DeviceInfo dev;
+  if (mpk::device_info(&dev) != cudaSuccess) return 0;
+  // The scalar path (unaligned grads) uses the most blocks for a given n.
+  return sizeof(double) * static_cast<size_t>(mpk::norm_blocks(n, false, dev));
+}
+
+int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip, void* workspace, size_t workspace_bytes,
+                 float* d_norm, float* d_scale, double* d_sumsq, void* stream) {
+  if ((n != 0 && grads == nullptr) || d_norm == nullptr || d_scale == nullptr) return MP_ERR_NULL;
+  if (workspace == nullptr) return MP_ERR_WORKSPACE;
+  if (!aligned(grads, 2) || !aligned(workspace, 8) || !aligned(d_norm, 4) || !aligned(d_scale, 4) ||
+      !aligned(d_sumsq, 8))
+    return MP_ERR_ALIGN;
+  if (!(clip > 0.0f) || !std::isfinite(clip) || n > kMaxN) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(grads, 16);
+  const int nb = mpk::norm_blocks(n, vec, dev);
+  if (workspace_bytes < sizeof(double) * static_cast<size_t>(nb)) return MP_ERR_WORKSPACE;
+  e = mpk::launch_norm(grads, n, vec, static_cast<double*>(workspace), nb, clip, d_norm, d_scale, d_sumsq,
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
+                  uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                  float lr, float beta1, float beta2, float eps, float weight_decay, const float* d_grad_scale,
+                  int32_t t, uint32_t seed, int32_t* d_status, void* stream) {
+  if (n == 0) return MP_OK;
+  if (params == nullptr || grads == nullptr || m == nullptr || v == nullptr || table == nullptr)
+    return MP_ERR_NULL;
+  if (!aligned(params, 2) || !aligned(grads, 2) || !aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) ||
+      !aligned(d_grad_scale, 4) || !aligned(d_status, 4))
+    return MP_ERR_ALIGN;
+  if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay) || !(beta1 >= 0.0f) ||
+      !(beta1 < 1.0f) || !(beta2 >= 0.0f) || !(beta2 < 1.0f) || t < 1)
+    return MP_ERR_RANGE;
+  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
+  if (n_tensors < 1) return MP_ERR_TABLE;
+
+  // The table must tile [0, total) contiguously and cover the range.
+  uint64_t off = 0;
+  for (int32_t k = 0; k < n_tensors; ++k) {
+    const mp_tensor_t& T = table[k];
+    if (T.offset != off || T.size > kMaxN || (T.decay != 0 && T.decay != 1) || T.reserved != 0)
+      return MP_ERR_TABLE;
+    off += T.size;
+    if (off > kMaxN) return MP_ERR_TABLE;
+  }
+  const uint64_t lo = global_offset, hi = global_offset + n;
+  if (off < hi) return MP_ERR_TABLE;
+
+  // Decay segments over [lo, hi): maximal runs of equal flag, so flags alternate.
+  std::vector<uint64_t> seg_end;
+  std::vector<int> seg_flag;
+  for (int32_t k = 0; k < n_tensors; ++k) {
+    const uint64_t a = table[k].offset, b = table[k].offset + table[k].size;
+    if (b <= lo || a >= hi || a == b) continue;
+    const uint64_t end = b < hi ? b : hi;
+    if (!seg_flag.empty() && seg_flag.back() == table[k].decay) {
+      seg_end.back() = end;
+    } else {
+      seg_end.push_back(end);
+      seg_flag.push_back(table[k].decay);
+    }
+  }
+
+  mpk::StepArgs base{};
+  base.d_scale = d_grad_scale;
+  base.d_status = d_status;
+  base.lr = lr;
+  base.beta1 = beta1;
+  base.beta2 = beta2;
+  base.eps = eps;
+  base.wd = weight_decay;
+  base.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(t)));
+  base.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(t)));
+  base.seed = seed;
+
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(params, 8) && aligned(grads, 8) && aligned(master, 16) && aligned(m, 16) &&
+                   aligned(v, 16);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // One launch per chunk of at most kSegCapLarge segments; chunk starts stay
+  // multiples of 4 elements from `lo` so vector alignment is preserved.
+  const size_t ns = seg_end.size();
+  uint64_t c0 = lo;
+  size_t s0 = 0;
+  while (c0 < hi) {
+    uint64_t c1 = hi;
+    size_t last = ns - 1;
+    if (ns - s0 > mpk::kSegCapLarge) {
+      // Cut at the start of segment s0 + CAP - 1, rounded down to a multiple
+      // of 4 from lo. Segments s0+1 .. s0+CAP-2 hold >= 1 element each, so the
+      // chunk keeps >= 1020 elements and at most CAP - 1 segments.
+      const uint64_t cut = seg_end[s0 + mpk::kSegCapLarge - 2];
+      c1 = lo + ((cut - lo) & ~static_cast<uint64_t>(3));
+      last = s0;
+      while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
+    }
+    mpk::StepArgs a = base;
+    const uint64_t d = c0 - lo;
+    a.params = params + d;
+    a.grads = grads + d;
+    a.master = master ? master + d : nullptr;
+    a.m = m + d;
+    a.v = v + d;
+    a.n = c1 - c0;
+    a.goff = c0;
+    a.nseg = static_cast<uint32_t>(last - s0 + 1);
+    a.first_decay = static_cast<uint32_t>(seg_flag[s0]);
+    std::vector<uint64_t> ends(seg_end.begin() + s0, seg_end.begin() + last + 1);
+    ends.back() = c1;
+    e = mpk::launch_adamw(a, ends.data(), vec, dev, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c0 = c1;
+    while (s0 < ns && seg_end[s0] <= c0) ++s0;
+  }
+  return MP_OK;
+}
+
+int mp_stochastic_round(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n, uint32_t seed,
+                        void* stream) {
+  if (n == 0) return MP_OK;
+  if (out == nullptr || in == nullptr) return MP_ERR_NULL;
+  if (!aligned(out, 2) || !aligned(in, 4)) return MP_ERR_ALIGN;
+  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(in, 16) && aligned(out, 8);
+  e = mpk::launch_sr(out, in, global_offset, n, seed, vec, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n, uint32_t seed, void* stream) {
+  if (n == 0) return MP_OK;
+  if (out == nullptr) return MP_ERR_NULL;
+  if (!aligned(out, 4)) return MP_ERR_ALIGN;
+  if (n > kMaxN) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = mpk::launch_noise(out, first_index, n, seed, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+}  // extern "C"

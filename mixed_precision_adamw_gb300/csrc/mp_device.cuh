@@ -1,0 +1,86 @@
+// mp_device.cuh — device-side building blocks of the optimizer step.
+//
+// Sources (web pages, by title and section):
+//   llm.c walk-through ch. 04 "Multi-GPU and mixed precision": §2.2 AdamW
+//   kernel (per-parameter update, two-FMA lerp), §2.3 stochastic rounding
+//   with SquirrelNoise5 draws.
+//
+// All floating-point operations are written as explicit round-to-nearest
+// intrinsics so that no FMA contraction or fast-math rewrite can change a
+// result: the update is bit-reproducible and matches its written definition.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mpk {
+
+constexpr int kThreads = 256;          // threads per block in every kernel
+constexpr int kGroup = 4;              // consecutive elements per fp32 16-B vector
+constexpr int kTile = kThreads * kGroup * 2;  // elements per block-iteration (two groups per thread)
+
+// ---- rounding randomness ---------------------------------------------------
+// SquirrelNoise5 (Squirrel Eiserloh's published counter-based noise hash) in
+// its 2D form, evaluated at x = low word, y = high word of the 64-bit global
+// element index. A pure function of (index, seed): independent of the grid.
+__device__ __forceinline__ uint32_t noise_u32(uint64_t k, uint32_t seed) {
+  const uint32_t x = static_cast<uint32_t>(k);
+  const uint32_t y = static_cast<uint32_t>(k >> 32);
+  uint32_t h = x + 198491317u * y;
+  h *= 0xD2A80A3Fu;
+  h += seed;
+  h ^= h >> 9;
+  h += 0xA884F197u;
+  h ^= h >> 11;
+  h *= 0x6C736F4Bu;
+  h ^= h >> 13;
+  h += 0xB79F3ABBu;
+  h ^= h >> 15;
+  h *= 0x1B56C4F5u;
+  h ^= h >> 17;
+  return h;
+}
+
+// ---- stochastic rounding fp32 -> bf16 -------------------------------------
+// Keep the top half of the fp32 pattern and add one (the bf16 neighbour away
+// from zero) when the discarded low half exceeds a uniform 16-bit draw, so
+// the probability of rounding away from zero is lo16 / 65536. NaN becomes
+// the canonical quiet NaN (truncation could otherwise yield an infinity).
+__device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t rand16) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t up = (b & 0xFFFFu) > rand16 ? 1u : 0u;
+  const uint32_t r = (b >> 16) + up;
+  return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+// ---- the per-element AdamW update ------------------------------------------
+struct Hyper {
+  float lr, beta1, beta2, eps, wd, bc1, bc2;
+};
+
+// lerp(start, end, w) = w * end + (start - w * start): two FMAs.
+__device__ __forceinline__ float lerp2(float start, float end, float w) {
+  return __fmaf_rn(w, end, __fmaf_rn(-w, start, start));
+}
+
+// Updates m and v in place and returns the new fp32 weight.
+//   g = scale * grad;  m = lerp(g, m, b1);  v = lerp(g*g, v, b2)
+//   p = old - lr * ( (m/bc1) / (sqrt(v/bc2) + eps) + wd_e * old )
+__device__ __forceinline__ float adamw_update(float grad, float& m, float& v, float old,
+                                              float wd_e, float scale, const Hyper& h) {
+  const float g = __fmul_rn(scale, grad);
+  m = lerp2(g, m, h.beta1);
+  const float gg = __fmul_rn(g, g);
+  v = lerp2(gg, v, h.beta2);
+  const float m_hat = __fdiv_rn(m, h.bc1);
+  const float v_hat = __fdiv_rn(v, h.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), h.eps);
+  const float update = __fadd_rn(__fdiv_rn(m_hat, denom), __fmul_rn(wd_e, old));
+  return __fsub_rn(old, __fmul_rn(h.lr, update));
+}
+
+}  // namespace mpk

@@ -1,0 +1,55 @@
+// mp_internal.h — host-side interface between the C ABI (mp_api.cu) and the
+// kernel launchers (mp_step.cu, mp_norm.cu, mp_sr.cu). Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mpk {
+
+// Decay segments: maximal runs of consecutive elements with the same decay
+// flag, passed to the step kernel by value (kernel parameter space). A launch
+// takes at most kSegCapLarge of them; the host splits longer tables into
+// several launches.
+constexpr uint32_t kSegCapSmall = 32;
+constexpr uint32_t kSegCapLarge = 1024;
+
+struct StepArgs {
+  uint16_t* params;
+  const uint16_t* grads;
+  float* master;  // nullptr: no-master variant
+  float* m;
+  float* v;
+  uint64_t n;     // elements in this launch
+  uint64_t goff;  // global index of element 0 of this launch
+  const float* d_scale;  // nullptr: scale 1
+  int32_t* d_status;     // may be nullptr
+  float lr, beta1, beta2, eps, wd, bc1, bc2;
+  uint32_t seed;
+  uint32_t nseg;         // segments covering [goff, goff + n)
+  uint32_t first_decay;  // decay flag of segment 0; flags alternate after it
+};
+
+struct DeviceInfo {
+  int device;
+  int sms;
+};
+
+cudaError_t device_info(DeviceInfo* out);
+
+// seg_end[s] = global index one past segment s; seg_end[nseg-1] == goff + n.
+cudaError_t launch_adamw(const StepArgs& a, const uint64_t* seg_end, bool vec,
+                         const DeviceInfo& dev, cudaStream_t stream);
+
+int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev);
+cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials,
+                        int nblocks, float clip, float* d_norm, float* d_scale,
+                        double* d_sumsq, cudaStream_t stream);
+
+cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
+                      uint32_t seed, bool vec, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_noise(uint32_t* out, uint64_t first, uint64_t n, uint32_t seed,
+                         const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace mpk

@@ -1,0 +1,159 @@
+// mp_norm.cu — deterministic global gradient norm and clip scale.
+//
+// llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §4: the train
+// step computes the global norm of all gradients with a two-level reduction
+// kernel, then grad_scale = min(1, 1.0 / grad_norm).
+//
+// Level 1 (norm_partial_kernel, persistent grid): each thread squares its
+// bf16 gradients in fp32 (exact for |g| in [2^-63, 2^64)), adds each 8-element
+// vector as a pairwise tree and accumulates the vector sums with Fast2Sum
+// compensation; the threads of a block are reduced in fp64 by a fixed
+// warp-shuffle tree and a fixed shared-memory pass. A block whose fp32 result
+// is non-finite or below 2^-60 (possible overflow or underflow of the fp32
+// squares) recomputes its share in fp64. Level 2 (norm_finalize_kernel, one
+// block) adds the per-block partials in a fixed order, takes the square root
+// and derives the clip scale on the device, so no host round trip is needed.
+// The grid depends only on n and the SM count: results are bit-identical
+// across runs.
+#include <cfloat>
+#include <cmath>
+
+#include "mp_device.cuh"
+#include "mp_internal.h"
+
+namespace mpk {
+namespace {
+
+constexpr int kNormBlocksPerSm = 8;  // 8 x 256 threads = a full SM
+constexpr int kUnroll = 4;           // 16-B loads in flight per thread
+
+__device__ __forceinline__ float sumsq8(uint4 w) {
+  const float a0 = bf16_lo(w.x), a1 = bf16_hi(w.x), a2 = bf16_lo(w.y), a3 = bf16_hi(w.y);
+  const float a4 = bf16_lo(w.z), a5 = bf16_hi(w.z), a6 = bf16_lo(w.w), a7 = bf16_hi(w.w);
+  const float s01 = __fadd_rn(__fmul_rn(a0, a0), __fmul_rn(a1, a1));
+  const float s23 = __fadd_rn(__fmul_rn(a2, a2), __fmul_rn(a3, a3));
+  const float s45 = __fadd_rn(__fmul_rn(a4, a4), __fmul_rn(a5, a5));
+  const float s67 = __fadd_rn(__fmul_rn(a6, a6), __fmul_rn(a7, a7));
+  return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+__device__ __forceinline__ double dsumsq8(uint4 w) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  double s = 0.0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const double lo = bf16_lo(ws[j]), hi = bf16_hi(ws[j]);
+    s = __dadd_rn(s, __dmul_rn(lo, lo));
+    s = __dadd_rn(s, __dmul_rn(hi, hi));
+  }
+  return s;
+}
+
+// s + x with the rounding error of the addition accumulated in c. Both terms
+// are non-negative, so max/min order them as Fast2Sum requires.
+__device__ __forceinline__ void acc(float& s, float& c, float x) {
+  const float t = __fadd_rn(s, x);
+  const float big = fmaxf(s, x), small = fminf(s, x);
+  c = __fadd_rn(c, __fadd_rn(__fsub_rn(big, t), small));
+  s = t;
+}
+
+// Fixed-order block sum in fp64; every thread receives the result.
+__device__ __forceinline__ double block_sum(double d, double* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d = __dadd_rn(d, __shfl_down_sync(0xFFFFFFFFu, d, o));
+  if (lane == 0) sh[warp] = d;
+  __syncthreads();
+  if (warp == 0) {
+    double r = lane < kThreads / 32 ? sh[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = __dadd_rn(r, __shfl_down_sync(0xFFFFFFFFu, r, o));
+    if (lane == 0) sh[kThreads / 32] = r;
+  }
+  __syncthreads();
+  const double r = sh[kThreads / 32];
+  __syncthreads();  // sh may be reused by the caller
+  return r;
+}
+
+// vec: grads 16-B aligned, processed as 8-element vectors plus a scalar tail.
+__global__ void __launch_bounds__(kThreads)
+norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, double* __restrict__ partials) {
+  __shared__ double sh[kThreads / 32 + 1];
+  const uint4* g4 = reinterpret_cast<const uint4*>(grads);
+  const uint64_t nvec = vec ? n / 8 : 0;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  const uint64_t k0 = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
+
+  float s = 0.0f, c = 0.0f;
+  uint64_t k = k0;
+  for (; k + (kUnroll - 1) * stride < nvec; k += kUnroll * stride) {
+    uint4 w[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) w[u] = __ldcs(g4 + k + u * stride);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) acc(s, c, sumsq8(w[u]));
+  }
+  for (; k < nvec; k += stride) acc(s, c, sumsq8(__ldcs(g4 + k)));
+  for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
+    const float x = bf16_to_f32(grads[i]);
+    acc(s, c, __fmul_rn(x, x));
+  }
+  double S = block_sum(__dadd_rn(static_cast<double>(s), static_cast<double>(c)), sh);
+
+  if (!(S <= DBL_MAX) || S < 0x1p-60) {  // uniform across the block: S is a broadcast value
+    double d = 0.0;
+    for (k = k0; k < nvec; k += stride) d = __dadd_rn(d, dsumsq8(__ldcs(g4 + k)));
+    for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
+      const double x = bf16_to_f32(grads[i]);
+      d = __dadd_rn(d, __dmul_rn(x, x));
+    }
+    S = block_sum(d, sh);
+  }
+  if (threadIdx.x == 0) partials[blockIdx.x] = S;
+}
+
+__global__ void __launch_bounds__(kThreads)
+norm_finalize_kernel(const double* __restrict__ partials, int nb, float clip,
+                     float* d_norm, float* d_scale, double* d_sumsq) {
+  __shared__ double sh[kThreads / 32 + 1];
+  double d = 0.0;
+  for (int i = threadIdx.x; i < nb; i += kThreads) d = __dadd_rn(d, partials[i]);
+  const double S = block_sum(d, sh);
+  if (threadIdx.x == 0) {
+    const float norm = __double2float_rn(__dsqrt_rn(S));
+    float scale;
+    if (!isfinite(norm)) {
+      scale = __int_as_float(0x7FC00000);  // NaN: the step refuses to run
+    } else {
+      const float q = __fdiv_rn(clip, norm);  // norm == 0 gives +Inf -> 1
+      scale = q < 1.0f ? q : 1.0f;
+    }
+    *d_norm = norm;
+    *d_scale = scale;
+    if (d_sumsq != nullptr) *d_sumsq = S;
+  }
+}
+
+}  // namespace
+
+int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev) {
+  const uint64_t items = vec ? (n / 8 > 0 ? n / 8 : n) : n;
+  uint64_t blocks = (items + kThreads - 1) / kThreads;
+  const uint64_t cap = static_cast<uint64_t>(dev.sms) * kNormBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials, int nblocks,
+                        float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream) {
+  norm_partial_kernel<<<nblocks, kThreads, 0, stream>>>(grads, n, vec ? 1 : 0, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  norm_finalize_kernel<<<1, kThreads, 0, stream>>>(partials, nblocks, clip, d_norm, d_scale, d_sumsq);
+  return cudaGetLastError();
+}
+
+}  // namespace mpk

@@ -1,0 +1,83 @@
+// mp_sr.cu — standalone stochastic rounding fp32 -> bf16 and the rounding
+// randomness itself.
+//
+// llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §2.3 (the rule)
+// and §5.2 (bf16 weights are rebuilt from the fp32 master with the saved
+// rounding randomness, so a resumed run is bit-identical). Because the draw is
+// keyed on the global element index, the rebuild needs no launch-geometry
+// alignment: any grid gives the same bits. HBM-bound: 6 B per element.
+#include "mp_device.cuh"
+#include "mp_internal.h"
+
+namespace mpk {
+namespace {
+
+constexpr int kSrBlocksPerSm = 8;
+
+// Vector path: in 16-B aligned, out 8-B aligned. Same tiling as the step:
+// thread t converts the 4-element groups at tile offsets 4t and 4t + 1024.
+__global__ void __launch_bounds__(kThreads)
+sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n, uint32_t seed) {
+  const uint64_t ntiles = n / kTile;
+  for (uint64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const uint64_t e0 = tile * kTile + threadIdx.x * kGroup;
+    const uint64_t e1 = e0 + kThreads * kGroup;
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(in + e0));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(in + e1));
+    const uint64_t k0 = goff + e0, k1 = goff + e1;
+    uint2 qa, qb;
+    qa.x = sr_bf16(a.x, noise_u32(k0 + 0, seed) & 0xFFFFu) | (sr_bf16(a.y, noise_u32(k0 + 1, seed) & 0xFFFFu) << 16);
+    qa.y = sr_bf16(a.z, noise_u32(k0 + 2, seed) & 0xFFFFu) | (sr_bf16(a.w, noise_u32(k0 + 3, seed) & 0xFFFFu) << 16);
+    qb.x = sr_bf16(b.x, noise_u32(k1 + 0, seed) & 0xFFFFu) | (sr_bf16(b.y, noise_u32(k1 + 1, seed) & 0xFFFFu) << 16);
+    qb.y = sr_bf16(b.z, noise_u32(k1 + 2, seed) & 0xFFFFu) | (sr_bf16(b.w, noise_u32(k1 + 3, seed) & 0xFFFFu) << 16);
+    __stcs(reinterpret_cast<uint2*>(out + e0), qa);
+    __stcs(reinterpret_cast<uint2*>(out + e1), qb);
+  }
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = ntiles * kTile + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint16_t>(sr_bf16(in[i], noise_u32(goff + i, seed) & 0xFFFFu));
+}
+
+__global__ void __launch_bounds__(kThreads)
+sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n, uint32_t seed) {
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint16_t>(sr_bf16(in[i], noise_u32(goff + i, seed) & 0xFFFFu));
+}
+
+__global__ void __launch_bounds__(kThreads)
+noise_kernel(uint32_t* __restrict__ out, uint64_t first, uint64_t n, uint32_t seed) {
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = noise_u32(first + i, seed);
+}
+
+unsigned grid_for(uint64_t units, const DeviceInfo& dev) {
+  uint64_t blocks = (units + kThreads - 1) / kThreads;
+  const uint64_t cap = static_cast<uint64_t>(dev.sms) * kSrBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n, uint32_t seed, bool vec,
+                      const DeviceInfo& dev, cudaStream_t stream) {
+  if (vec) {
+    const uint64_t ntiles = n / kTile;
+    const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);
+    sr_vec_kernel<<<blocks, kThreads, 0, stream>>>(out, in, goff, n, seed);
+  } else {
+    sr_scalar_kernel<<<grid_for(n, dev), kThreads, 0, stream>>>(out, in, goff, n, seed);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_noise(uint32_t* out, uint64_t first, uint64_t n, uint32_t seed, const DeviceInfo& dev,
+                         cudaStream_t stream) {
+  noise_kernel<<<grid_for(n, dev), kThreads, 0, stream>>>(out, first, n, seed);
+  return cudaGetLastError();
+}
+
+}  // namespace mpk

@@ -1,0 +1,119 @@
+"""The C ABI library builds, loads and exports every declared symbol, and its
+host-side argument checks reject bad input before any device work (no GPU
+needed: every call here fails validation before it would touch CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def mp():
+    from mixed_precision_adamw_gb300 import build
+    build.build()
+    import mixed_precision_adamw_gb300 as mp
+    return mp
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^\s*(?:[A-Za-z_][\w\s\*]*?)\b(mp_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mp_grad_norm", "mp_adamw_step", "mp_stochastic_round", "mp_grad_norm_workspace_bytes",
+                     "mp_status_string", "mp_last_cuda_error", "mp_noise_u32", "mp_abi_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(mp):
+    lib = ctypes.CDLL(mp.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(mp):
+    assert mp.abi_version() == 1
+    for s in range(8):
+        assert mp.status_string(s).startswith("MP_")
+    assert "unknown" in mp.status_string(99)
+
+
+FAKE = 0x100000  # never dereferenced: each call below fails validation first
+
+
+def _step(mp, **kw):
+    args = dict(params=FAKE, grads=FAKE, master=FAKE, m=FAKE, v=FAKE, goff=0, n=100,
+                table=[(0, 100, 1)], lr=1e-3, b1=0.9, b2=0.95, eps=1e-8, wd=0.1, scale=FAKE, t=1, seed=1,
+                status=None)
+    args.update(kw)
+    tab = mp.TensorTable(args["table"]) if args["table"] is not None else None
+    return mp.lib().mp_adamw_step(args["params"], args["grads"], args["master"], args["m"], args["v"],
+                                  args["goff"], args["n"], tab.ctypes_array if tab else None,
+                                  tab.n_tensors if tab else 0, args["lr"], args["b1"], args["b2"], args["eps"],
+                                  args["wd"], args["scale"], args["t"], args["seed"], args["status"], None)
+
+
+def test_step_argument_checks(mp):
+    assert _step(mp, n=0) == mp.MP_OK
+    assert _step(mp, params=None) == mp.MP_ERR_NULL
+    assert _step(mp, m=None) == mp.MP_ERR_NULL
+    assert _step(mp, table=None) == mp.MP_ERR_NULL
+    assert _step(mp, params=FAKE + 1) == mp.MP_ERR_ALIGN
+    assert _step(mp, master=FAKE + 2) == mp.MP_ERR_ALIGN
+    assert _step(mp, scale=FAKE + 2) == mp.MP_ERR_ALIGN
+    assert _step(mp, t=0) == mp.MP_ERR_RANGE
+    assert _step(mp, b1=1.0) == mp.MP_ERR_RANGE
+    assert _step(mp, b2=-0.1) == mp.MP_ERR_RANGE
+    assert _step(mp, lr=float("nan")) == mp.MP_ERR_RANGE
+    assert _step(mp, eps=float("inf")) == mp.MP_ERR_RANGE
+    assert _step(mp, goff=(1 << 62), n=10) == mp.MP_ERR_RANGE
+    # table: gap, overlap, not from 0, bad flag, too short for the range
+    assert _step(mp, table=[(0, 50, 1), (51, 49, 0)]) == mp.MP_ERR_TABLE
+    assert _step(mp, table=[(0, 50, 1), (49, 51, 0)]) == mp.MP_ERR_TABLE
+    assert _step(mp, table=[(1, 100, 1)]) == mp.MP_ERR_TABLE
+    assert _step(mp, table=[(0, 100, 2)]) == mp.MP_ERR_TABLE
+    assert _step(mp, table=[(0, 99, 1)]) == mp.MP_ERR_TABLE
+    assert _step(mp, goff=50, n=51, table=[(0, 100, 1)]) == mp.MP_ERR_TABLE
+    assert _step(mp, table=[]) == mp.MP_ERR_NULL or _step(mp, table=[]) == mp.MP_ERR_TABLE
+
+
+def test_norm_and_sr_argument_checks(mp):
+    L = mp.lib()
+    assert L.mp_grad_norm(None, 10, 1.0, FAKE, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_NULL
+    assert L.mp_grad_norm(FAKE, 10, 1.0, None, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_WORKSPACE
+    assert L.mp_grad_norm(FAKE, 10, 1.0, FAKE, 4096, None, FAKE, None, None) == mp.MP_ERR_NULL
+    assert L.mp_grad_norm(FAKE + 1, 10, 1.0, FAKE, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_ALIGN
+    assert L.mp_grad_norm(FAKE, 10, 1.0, FAKE + 4, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_ALIGN
+    assert L.mp_grad_norm(FAKE, 10, 0.0, FAKE, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+    assert L.mp_grad_norm(FAKE, 10, float("inf"), FAKE, 4096, FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+    assert L.mp_stochastic_round(None, FAKE, 0, 10, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_stochastic_round(FAKE + 1, FAKE, 0, 10, 1, None) == mp.MP_ERR_ALIGN
+    assert L.mp_stochastic_round(FAKE, FAKE + 2, 0, 10, 1, None) == mp.MP_ERR_ALIGN
+    assert L.mp_stochastic_round(FAKE, FAKE, (1 << 62), 10, 1, None) == mp.MP_ERR_RANGE
+    assert L.mp_stochastic_round(FAKE, FAKE, 0, 0, 1, None) == mp.MP_OK
+    assert L.mp_noise_u32(None, 0, 10, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_noise_u32(FAKE + 2, 0, 10, 1, None) == mp.MP_ERR_ALIGN
+
+
+def test_product_never_touches_the_oracle():
+    """The CUDA path and the oracle share no code: the package neither
+    imports, links nor names the oracle."""
+    pkg = os.path.join(ROOT, "mixed_precision_adamw_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, fn)).read().lower()
+                assert "oracle" not in text, f"{fn} mentions the oracle"
+    for fn in os.listdir(os.path.join(ROOT, "oracle")):
+        if fn.endswith((".c", ".h", ".py")):
+            text = open(os.path.join(ROOT, "oracle", fn)).read()
+            assert "mixed_precision_adamw_gb300" not in text and "mp_adamw.h" not in text

@@ -1,0 +1,433 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every test runs the library's kernels on a GB300 and compares element by
+element with the oracle on the same seeded inputs, at the bars listed in
+tests/helpers.py. Sizes span several 2048-element tiles plus ragged tails;
+full-size parameter sets are checked in full (GPT-2 124M) or on windows the
+oracle recomputes with their global offsets (GPT-2 1.5B, Llama-3-8B).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import (assert_bf16_close, assert_bit_equal, assert_f32_close, rel_err, to_np_f32,
+                     to_np_u16)
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import mixed_precision_adamw_gb300 as mp
+else:  # collected on CPU machines, skipped below
+    mp = None
+
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    yield
+    torch.cuda.synchronize()
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def bf16_from_f32(x: np.ndarray) -> np.ndarray:
+    return W.bf16_bits(torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16))
+
+
+def dev_u16(a: np.ndarray, pad: int = 0) -> torch.Tensor:
+    """Device bf16 tensor holding raw patterns a, optionally starting `pad`
+    elements into a larger buffer (pad odd -> only 2-B aligned)."""
+    buf = torch.empty(a.size + pad, dtype=torch.int16, device=DEV)
+    out = buf[pad:]
+    out.copy_(torch.from_numpy(a.view(np.int16)))
+    return out.view(torch.bfloat16)
+
+
+def dev_f32(a: np.ndarray, pad: int = 0) -> torch.Tensor:
+    buf = torch.empty(a.size + pad, dtype=torch.float32, device=DEV)
+    out = buf[pad:]
+    out.copy_(torch.from_numpy(np.ascontiguousarray(a, np.float32)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# rounding randomness and stochastic rounding: bit-exact
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("first,seed,n", [(0, 0, 1 << 20), (123456789, 42, 1000003),
+                                          ((1 << 32) - 5000, 7, 10000), ((5 << 32) + 3, 2024, 77777)])
+def test_noise_bit_exact(first, seed, n):
+    out = torch.empty(n, dtype=torch.int32, device=DEV)
+    mp.mp_noise_u32(out, first, seed)
+    got = out.cpu().numpy().view(np.uint32)
+    assert_bit_equal(got, oracle.noise_fill(first, n, seed), "noise")
+
+
+def _special_f32(n, rng):
+    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-45, 38, n)).astype(np.float32)
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, np.finfo(np.float32).max,
+                         -np.finfo(np.float32).max, 1e-45, -1e-45, 1.17549435e-38, 257.0, 1.0 + 2 ** -8],
+                        np.float32)
+    x[: specials.size] = specials
+    # NaNs with low payload bits only, and bf16-representable values
+    x[specials.size:specials.size + 4] = np.array([0x7F800001, 0xFF800003, 0x7FC00000, 0x7F80FFFF],
+                                                  np.uint32).view(np.float32)
+    x[-1000:] = (x[-1000:].view(np.uint32) & 0xFFFF0000).view(np.float32)
+    return x
+
+
+@pytest.mark.parametrize("n,pad_in,pad_out,goff", [
+    (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32),
+    (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000)])
+def test_stochastic_round_bit_exact(n, pad_in, pad_out, goff):
+    rng = np.random.default_rng(n + pad_in)
+    x = _special_f32(n, rng) if n > 2000 else rng.standard_normal(n).astype(np.float32)
+    xin = dev_f32(x, pad_in)
+    out = dev_u16(np.zeros(n, np.uint16), pad_out)
+    seed = 0xC0FFEE
+    mp.mp_stochastic_round(out, xin, seed, global_offset=goff)
+    assert_bit_equal(to_np_u16(out), oracle.stochastic_round(x, goff, seed), "sr")
+
+
+def test_stochastic_round_full_size_and_drift():
+    """SR stress: 64M fp32 weights with |w| log-uniform in [1e-3, 1e1]; a
+    constant update of 1e-4 |w| per step for 1000 steps. SR (bit-exact
+    against the oracle on the same fp32 inputs) tracks the fp32 trajectory;
+    round-to-nearest never moves."""
+    n = 64 << 20
+    w0 = W.sr_stress_weights(n, device=DEV)
+    delta = (w0.abs() * f32(1e-4)).float()
+    x = w0.clone()
+    out = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    mp.mp_stochastic_round(out, x, W.step_seed(0))
+    xs = to_np_f32(x)
+    assert_bit_equal(to_np_u16(out), oracle.stochastic_round(xs, 0, W.step_seed(0)), "sr 64M")
+    fp32 = w0.clone()
+    sr = w0.to(torch.bfloat16)
+    for t in range(1, 1001):
+        fp32 += delta
+        torch.add(sr.float(), delta, out=x)
+        mp.mp_stochastic_round(sr, x, W.step_seed(t))
+        if t in (1, 500):
+            idx = slice(12345678, 12345678 + (1 << 20))
+            assert_bit_equal(to_np_u16(sr[idx]), oracle.stochastic_round(to_np_f32(x[idx]), 12345678,
+                                                                         W.step_seed(t)), f"sr step {t}")
+    rne = w0.to(torch.bfloat16).float()
+    drift_sr = float((sr.float().double() / fp32.double() - 1.0).mean())
+    drift_rne = float((rne.double() / fp32.double() - 1.0).mean())
+    expect_rne = float(torch.where(w0 > 0, 1 / 1.1 - 1, 1 / 0.9 - 1).double().mean())
+    assert abs(drift_rne - expect_rne) < 1e-3
+    assert abs(drift_sr) < 1e-4, drift_sr
+
+
+# ---------------------------------------------------------------------------
+# gradient norm
+# ---------------------------------------------------------------------------
+def _norm_gpu(g: torch.Tensor, clip=1.0):
+    n = g.numel()
+    ws = torch.empty(max(8, mp.mp_grad_norm_workspace_bytes(n)), dtype=torch.uint8, device=DEV)
+    d_norm = torch.empty(1, dtype=torch.float32, device=DEV)
+    d_scale = torch.empty(1, dtype=torch.float32, device=DEV)
+    d_sumsq = torch.empty(1, dtype=torch.float64, device=DEV)
+    mp.mp_grad_norm(g, clip, ws, d_norm, d_scale, d_sumsq)
+    return float(d_sumsq.item()), np.float32(d_norm.item()), np.float32(d_scale.item())
+
+
+@pytest.mark.parametrize("n,pad", [(0, 0), (1, 0), (7, 0), (8, 0), (2047, 1), (2048 * 5 + 3, 0),
+                                   (1000003, 0), (1000003, 3), (1 << 24, 0)])
+def test_grad_norm_parity(n, pad):
+    rng = np.random.default_rng(n)
+    g = bf16_from_f32(rng.standard_normal(n) * 10.0 ** rng.uniform(-5, 1, n))
+    s, nrm, sc = _norm_gpu(dev_u16(g, pad))
+    s_o, nrm_o, sc_o = oracle.grad_norm(g, 1.0)
+    if n == 0:
+        assert s == 0.0 and nrm == 0 and sc == 1.0
+        return
+    assert rel_err(s, s_o) <= 1e-6
+    assert rel_err(float(nrm), math.sqrt(s_o)) <= 1e-6
+    assert sc == oracle.clip_scale(float(nrm), 1.0)  # the scale rule is exact given the norm
+    # bit-identical on repeated runs
+    for _ in range(3):
+        assert _norm_gpu(dev_u16(g, pad)) == (s, nrm, sc)
+
+
+@pytest.mark.parametrize("case", ["tiny", "huge", "mixed", "zeros", "subnormal"])
+def test_grad_norm_extreme_ranges(case):
+    rng = np.random.default_rng(5)
+    n = 3 * 2048 * 152 + 11
+    if case == "tiny":
+        x = rng.standard_normal(n) * 1e-30
+    elif case == "huge":
+        x = rng.standard_normal(n) * 1e25
+    elif case == "mixed":
+        x = rng.standard_normal(n) * 10.0 ** rng.uniform(-35, 30, n)
+    elif case == "zeros":
+        x = np.zeros(n)
+    else:
+        x = rng.standard_normal(n) * 1e-39
+    g = bf16_from_f32(x)
+    s, nrm, sc = _norm_gpu(dev_u16(g), clip=1.0)
+    s_o, nrm_o, sc_o = oracle.grad_norm(g, 1.0)
+    assert rel_err(s, s_o) <= 1e-6, (s, s_o)
+    assert rel_err(float(nrm), float(nrm_o)) <= 1e-6
+    assert sc == oracle.clip_scale(float(nrm), 1.0)
+
+
+def test_grad_norm_nonfinite():
+    g = bf16_from_f32(np.ones(100000))
+    for bad in (0x7FC0, 0x7F80, 0xFF80):
+        g2 = g.copy()
+        g2[77777] = bad
+        s, nrm, sc = _norm_gpu(dev_u16(g2))
+        assert not math.isfinite(nrm) and math.isnan(sc)
+
+
+# ---------------------------------------------------------------------------
+# the AdamW + SR step
+# ---------------------------------------------------------------------------
+class State:
+    def __init__(self, params, grads, master, m, v):
+        self.params, self.grads, self.master, self.m, self.v = params, grads, master, m, v
+
+
+def _host_state(st):
+    return dict(params=W.bf16_bits(st["params"].cpu()).copy(), master=st["master"].cpu().numpy().copy()
+                if "master" in st else None, m=st["m"].cpu().numpy().copy(), v=st["v"].cpu().numpy().copy())
+
+
+def _compare(gpu_st, host, name, exact=True):
+    assert_bf16_close(to_np_u16(gpu_st["params"]), host["params"], f"{name} params")
+    for k in ("master", "m", "v"):
+        if host.get(k) is not None:
+            assert_f32_close(to_np_f32(gpu_st[k]), host[k], f"{name} {k}")
+    if exact:
+        assert_bit_equal(to_np_u16(gpu_st["params"]), host["params"], f"{name} params (bitwise)")
+        for k in ("master", "m", "v"):
+            if host.get(k) is not None:
+                assert_bit_equal(to_np_f32(gpu_st[k]), host[k], f"{name} {k} (bitwise)")
+
+
+def _run_steps(name, steps, with_master, device_state=None):
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    H = W.HYPER
+    st = W.make_state(name, device="cpu", with_master=with_master)
+    host = _host_state(st)
+    dst = {k: t.to(DEV) for k, t in st.items()}
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"])
+    for t in range(1, steps + 1):
+        g = W.make_grads(name, t)
+        gb = W.bf16_bits(g).copy()
+        dg = g.to(DEV)
+        opt.step(dst["params"], dg, dst.get("master"), dst["m"], dst["v"], t, W.step_seed(t))
+        s_o, nrm_o, sc_o = oracle.grad_norm(gb, H["clip"])
+        st_o = oracle.adamw_step(host["params"], gb, host["master"], host["m"], host["v"], 0, tab, H["lr"],
+                                 H["beta1"], H["beta2"], H["eps"], H["weight_decay"],
+                                 float(opt.d_scale.item()), t, W.step_seed(t))
+        assert st_o == 0
+        opt.check_status()
+        assert rel_err(float(opt.d_norm.item()), float(nrm_o)) <= 1e-6
+        assert float(opt.d_scale.item()) == oracle.clip_scale(float(opt.d_norm.item()), H["clip"])
+        _compare(dst, host, f"{name} step {t}")
+    return dst, host
+
+
+@pytest.mark.parametrize("with_master", [True, False])
+def test_tiny_sixteen_steps(with_master):
+    _run_steps("tiny", 16, with_master)
+
+
+@pytest.mark.parametrize("with_master", [True, False])
+def test_gpt2_124m_full_parity(with_master):
+    _run_steps("gpt2_124m", 2, with_master)
+
+
+def _random_case(n, seed, tmin=1, tmax=5000):
+    gen = torch.Generator().manual_seed(seed)
+    tab = W.random_table(n, gen, tmin, tmax)
+    rng = np.random.default_rng(seed)
+    master = (rng.standard_normal(n) * 0.05).astype(np.float32)
+    params = bf16_from_f32(master)
+    m = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    v = (rng.random(n) * 1e-6).astype(np.float32)
+    grads = bf16_from_f32(rng.standard_normal(n) * 1e-2)
+    return tab, params, grads, master, m, v
+
+
+@pytest.mark.parametrize("n,pad,with_master,tmax", [
+    (2048 * 9 + 1234, 0, True, 5000), (2048 * 9 + 1234, 0, False, 5000), (2048 * 9 + 1234, 1, True, 5000),
+    (5, 0, True, 3), (2048, 0, True, 1), (2048 * 3 + 1, 2, False, 2), (700000, 0, True, 40),
+    (1 << 20, 0, True, 1 << 20)])
+def test_step_random_tables(n, pad, with_master, tmax):
+    tab, params, grads, master, m, v = _random_case(n, n + pad, 1, tmax)
+    lr, b1, b2, eps, wd, scale, t, seed = 3e-3, 0.9, 0.95, 1e-8, 0.1, 0.37, 7, 99
+    d = dict(params=dev_u16(params, pad), grads=dev_u16(grads, pad), m=dev_f32(m, pad), v=dev_f32(v, pad),
+             master=dev_f32(master, pad) if with_master else None)
+    d_scale = torch.tensor([scale], dtype=torch.float32, device=DEV)
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=lr, beta1=b1,
+                     beta2=b2, eps=eps, weight_decay=wd, d_grad_scale=d_scale, t=t, seed=seed)
+    host = dict(params=params.copy(), master=master.copy() if with_master else None, m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, lr, b1, b2, eps,
+                             wd, f32(scale), t, seed) == 0
+    _compare(d, host, f"random n={n}")
+
+
+def test_step_many_segments_split_into_launches():
+    """A table with 5000 alternating-decay tensors (more segments than one
+    launch carries) gives the same result as the oracle."""
+    n = 5000 * 37
+    tab = [(k * 37, 37, k % 2) for k in range(5000)]
+    _, params, grads, master, m, v = _random_case(n, 3)
+    d = dict(params=dev_u16(params), grads=dev_u16(grads), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master))
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=1e-2,
+                     beta1=0.9, beta2=0.99, eps=1e-8, weight_decay=0.5, d_grad_scale=None, t=3, seed=5)
+    host = dict(params=params.copy(), master=master.copy(), m=m.copy(), v=v.copy())
+    oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, 1e-2, 0.9, 0.99, 1e-8,
+                      0.5, 1.0, 3, 5)
+    _compare(d, host, "5000 segments")
+
+
+def test_shard_launches_equal_whole_buffer_and_oracle_windows():
+    """GPT-2 1.5B shapes (1,557,686,400 params): the whole-buffer step and 8
+    contiguous shard launches (the ZeRO-1 layout, no communication) are
+    bit-identical; windows are checked against the oracle."""
+    name = "gpt2_1558m"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    N = W.total(entries)
+    H = W.HYPER
+    st = W.make_state(name, device=DEV)
+    g = W.make_grads(name, 1, device=DEV)
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"])
+    windows = [(0, 1 << 16), (N // 2 - 4099, 1 << 16), (N - 70001, 70001)]
+    for k in range(1, 8):
+        windows.append((k * (N // 8) - 3000, 6000))
+    before = {k: [(to_np_u16(st["params"][a:a + n]) if k == "params" else to_np_f32(st[k][a:a + n]))
+                  for a, n in windows] for k in st}
+    gwin = [to_np_u16(g[a:a + n]) for a, n in windows]
+    mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale)
+    shard = {k: t.clone() for k, t in st.items()}
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"],
+              d_grad_scale=opt.d_scale, t=1, seed=W.step_seed(1))
+    mp.mp_adamw_step(st["params"], g, st["master"], st["m"], st["v"], opt.table, **kw)
+    per = N // 8
+    for r in range(8):
+        sl = slice(r * per, (r + 1) * per)
+        mp.mp_adamw_step(shard["params"][sl], g[sl], shard["master"][sl], shard["m"][sl], shard["v"][sl],
+                         opt.table, global_offset=r * per, **kw)
+    torch.cuda.synchronize()
+    for k in st:
+        assert torch.equal(st[k].view(torch.int16) if k == "params" else st[k].view(torch.int32),
+                           shard[k].view(torch.int16) if k == "params" else shard[k].view(torch.int32)), k
+    scale = float(opt.d_scale.item())
+    for i, (a, n) in enumerate(windows):
+        host = {k: before[k][i].copy() for k in before}
+        assert oracle.adamw_step(host["params"], gwin[i], host["master"], host["m"], host["v"], a, tab, H["lr"],
+                                 H["beta1"], H["beta2"], H["eps"], H["weight_decay"], scale, 1, W.step_seed(1)) == 0
+        _compare({k: st[k][a:a + n] for k in st}, host, f"1.5B window {a}")
+
+
+@pytest.mark.slow
+def test_llama3_8b_windows():
+    """Llama-3-8B shapes (8,030,261,248 params, ~128 GB of state in HBM):
+    one full step; windows (including across the 2^32 index boundary) are
+    checked against the oracle; the norm against an fp64 sum over all grads."""
+    name = "llama3_8b"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    N = W.total(entries)
+    H = W.HYPER
+    st = W.make_state(name, device=DEV)
+    g = W.make_grads(name, 1, device=DEV)
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"])
+    windows = [(0, 1 << 16), ((1 << 32) - 50000, 100000), (N // 3, 1 << 16), (N - 100003, 100003)]
+    before = {k: [(to_np_u16(st["params"][a:a + n]) if k == "params" else to_np_f32(st[k][a:a + n]))
+                  for a, n in windows] for k in st}
+    gwin = [to_np_u16(g[a:a + n]) for a, n in windows]
+    opt.step(st["params"], g, st["master"], st["m"], st["v"], 1, W.step_seed(1))
+    torch.cuda.synchronize()
+    opt.check_status()
+    # norm: fp64 sum over every gradient, streamed in chunks through the oracle
+    s_o = 0.0
+    chunk = 1 << 28
+    for a in range(0, N, chunk):
+        s_o += oracle.sumsq(to_np_u16(g[a:min(N, a + chunk)]))
+    nrm = float(opt.d_norm.item())
+    assert rel_err(nrm, math.sqrt(s_o)) <= 1e-6
+    scale = float(opt.d_scale.item())
+    assert scale < 1.0
+    for i, (a, n) in enumerate(windows):
+        host = {k: before[k][i].copy() for k in before}
+        assert oracle.adamw_step(host["params"], gwin[i], host["master"], host["m"], host["v"], a, tab, H["lr"],
+                                 H["beta1"], H["beta2"], H["eps"], H["weight_decay"], scale, 1, W.step_seed(1)) == 0
+        _compare({k: st[k][a:a + n] for k in st}, host, f"8B window {a}")
+
+
+# ---------------------------------------------------------------------------
+# failure handling and memory safety
+# ---------------------------------------------------------------------------
+def test_nonfinite_norm_refuses_the_step():
+    n = 2048 * 4 + 3
+    tab, params, grads, master, m, v = _random_case(n, 11)
+    grads[1234] = 0x7FC0  # a NaN gradient
+    d = dict(params=dev_u16(params), grads=dev_u16(grads), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master))
+    opt = mp.Optimizer(tab, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip=1.0)
+    opt.step(d["params"], d["grads"], d["master"], d["m"], d["v"], 1, 1)
+    torch.cuda.synchronize()
+    assert math.isnan(float(opt.d_scale.item()))
+    with pytest.raises(mp.MpError) as ei:
+        opt.check_status()
+    assert ei.value.status == mp.MP_ERR_NONFINITE
+    assert_bit_equal(to_np_u16(d["params"]), params, "params untouched")
+    assert_bit_equal(to_np_f32(d["master"]), master, "master untouched")
+    assert_bit_equal(to_np_f32(d["m"]), m, "m untouched")
+    assert_bit_equal(to_np_f32(d["v"]), v, "v untouched")
+
+
+SENT16 = 0x5A5A
+SENT32 = 0x7F7FA5A5  # a NaN pattern nothing computes
+
+
+def _guarded(a: np.ndarray, pad: int, guard: int = 4096):
+    """Device copy of a with `guard` sentinel elements on each side; returns
+    (whole buffer, view of a)."""
+    if a.dtype == np.uint16:
+        buf = torch.full((a.size + pad + 2 * guard,), SENT16, dtype=torch.int16, device=DEV)
+        v = buf[guard + pad:guard + pad + a.size]
+        v.copy_(torch.from_numpy(a.view(np.int16)))
+        return buf, v.view(torch.bfloat16)
+    buf = torch.full((a.size + pad + 2 * guard,), SENT32, dtype=torch.int32, device=DEV)
+    v = buf[guard + pad:guard + pad + a.size]
+    v.copy_(torch.from_numpy(a.view(np.int32)))
+    return buf, v.view(torch.float32)
+
+
+def _check_guards(buf, n, pad, guard=4096):
+    h = buf.cpu().numpy().astype(np.int64)
+    sent = SENT16 if buf.dtype == torch.int16 else SENT32
+    assert np.all(h[:guard + pad] == sent) and np.all(h[guard + pad + n:] == sent), "guard band overwritten"
+
+
+@pytest.mark.parametrize("n,pad", [(1, 0), (2048 * 3 + 7, 0), (2048 * 3 + 7, 1), (4099, 3)])
+def test_guard_bands_untouched(n, pad):
+    tab, params, grads, master, m, v = _random_case(n, 21)
+    bufs = {k: _guarded(a, pad) for k, a in dict(params=params, grads=grads, master=master, m=m, v=v).items()}
+    views = {k: b[1] for k, b in bufs.items()}
+    opt = mp.Optimizer(tab, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip=1.0)
+    opt.step(views["params"], views["grads"], views["master"], views["m"], views["v"], 2, 9)
+    out_buf, out = _guarded(np.zeros(n, np.uint16), pad)
+    mp.mp_stochastic_round(out, views["master"], 4)
+    torch.cuda.synchronize()
+    for b, _ in list(bufs.values()) + [(out_buf, out)]:
+        _check_guards(b, n, pad)
