@@ -45,7 +45,7 @@ class MpTensor(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m mixed_precision_adamw_gb300.build` "
+            f"{LIB_PATH} is missing: build it with `python mixed_precision_adamw_gb300/build.py` "
             "(nvcc, sm_103a). There is no fallback path.")
     L = ctypes.CDLL(LIB_PATH)
     vp, u64, u32, i32, f32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32, ctypes.c_float

@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def mp():
-    from mixed_precision_adamw_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import mixed_precision_adamw_gb300 as mp
     return mp
 

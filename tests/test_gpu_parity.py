@@ -20,6 +20,8 @@ from helpers import (assert_bf16_close, assert_bit_equal, assert_f32_close, rel_
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
+    import __graft_entry__
+    __graft_entry__.build()  # no-op when the library is up to date
     import mixed_precision_adamw_gb300 as mp
 else:  # collected on CPU machines, skipped below
     mp = None
@@ -431,3 +433,38 @@ def test_guard_bands_untouched(n, pad):
     torch.cuda.synchronize()
     for b, _ in list(bufs.values()) + [(out_buf, out)]:
         _check_guards(b, n, pad)
+
+
+def test_resume_replay_is_bit_identical():
+    """llm.c ch. 04 §5.2: restore the fp32 master/m/v, rebuild the bf16
+    weights with mp_stochastic_round(master, seed of the last step), and the
+    continued run equals the uninterrupted one bit for bit."""
+    name = "gpt2_124m"
+    n_params = 1 << 22
+    from bench import prefix_entries
+    entries = prefix_entries(W.layout(W.specs_for(name)), n_params)
+    tab = W.table(entries)
+    H = W.HYPER
+    st0 = W.make_state(name, device=DEV, entries=entries)
+    grads = {t: W.make_grads(name, t, device=DEV, entries=entries) for t in range(1, 7)}
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"])
+
+    def run(s, t0, t1):
+        for t in range(t0, t1):
+            opt.step(s["params"], grads[t], s["master"], s["m"], s["v"], t, W.step_seed(t))
+
+    a = {k: x.clone() for k, x in st0.items()}
+    run(a, 1, 7)
+    b = {k: x.clone() for k, x in st0.items()}
+    run(b, 1, 4)
+    params_before = b["params"].clone()
+    b["params"].fill_(float("nan"))  # the checkpoint holds no bf16 weights
+    mp.mp_stochastic_round(b["params"], b["master"], W.step_seed(3))
+    assert torch.equal(b["params"].view(torch.int16), params_before.view(torch.int16))
+    run(b, 4, 7)
+    torch.cuda.synchronize()
+    opt.check_status()
+    for k in a:
+        assert torch.equal(a[k].view(torch.int16) if k == "params" else a[k].view(torch.int32),
+                           b[k].view(torch.int16) if k == "params" else b[k].view(torch.int32)), k

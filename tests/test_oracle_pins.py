@@ -468,3 +468,38 @@ def test_sr_tracks_small_updates_where_round_to_nearest_stalls():
     expect = float(np.mean(np.where(w0 > 0, 1 / 1.1 - 1, 1 / 0.9 - 1)))
     assert abs(rel_rne - expect) < 2e-3
     assert abs(rel_sr) < 2e-3  # SR follows the fp32 trajectory in expectation
+
+
+# --------------------------------------------------------------------------
+# Bit-perfect resume — llm.c ch. 04 §5.2: bf16 weights are not checkpointed;
+# they are rebuilt from the fp32 master with the saved rounding randomness.
+# With draws keyed on the global index, the rebuild is SR(master, seed_t).
+# --------------------------------------------------------------------------
+def test_resume_rebuilds_bf16_bit_identically():
+    name = "tiny"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    H = W.HYPER
+    st = W.make_state(name)
+    N = W.total(entries)
+
+    def fresh():
+        return dict(params=W.bf16_bits(st["params"]).copy(), master=st["master"].numpy().copy(),
+                    m=np.zeros(N, np.float32), v=np.zeros(N, np.float32))
+
+    def run(s, t0, t1):
+        for t in range(t0, t1):
+            g = W.bf16_bits(W.make_grads(name, t)).copy()
+            _, _, scale = oracle.grad_norm(g, H["clip"])
+            assert oracle.adamw_step(s["params"], g, s["master"], s["m"], s["v"], 0, tab, H["lr"], H["beta1"],
+                                     H["beta2"], H["eps"], H["weight_decay"], float(scale), t, W.step_seed(t)) == 0
+
+    a = fresh()
+    run(a, 1, 7)
+    b = fresh()
+    run(b, 1, 4)
+    ckpt = {k: b[k].copy() for k in ("master", "m", "v")}  # no bf16 weights saved
+    b = dict(ckpt, params=oracle.stochastic_round(ckpt["master"], 0, W.step_seed(3)))
+    run(b, 4, 7)
+    for k in a:
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
