@@ -200,6 +200,35 @@ int mp_stochastic_round(uint16_t* out, const float* in,
 int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n,
                  uint32_t seed, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Gradient norm without a workspace. The pages have no counterpart to this
+ * call: it exists for callers that cannot allocate device memory — a host
+ * framework that reserves all device memory in its own pool and hands a
+ * plugin only its input and output buffers, or a loop that cannot afford the
+ * device-wide synchronisation that cudaMalloc/cudaFree bring. It computes
+ * exactly what mp_grad_norm computes, with the same kernels and the same
+ * results, but keeps the per-block partial sums in a 32 KB scratch array the
+ * library itself defines in device memory (room for 4096 partials; every GPU
+ * that loads the library holds it until the process exits). Nothing is
+ * allocated on any call, by the library or by anything it calls.
+ *
+ *   grads, n, clip, d_norm, d_scale, d_sumsq, stream: as for mp_grad_norm.
+ *
+ * The first call on a device looks up the scratch array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture. The scratch is shared by all calls on a device and keeps
+ * the last call's contents (each call overwrites every slot it reads, so
+ * nothing needs clearing): calls that overlap on the GPU — on two streams,
+ * or from two threads without ordering — race on it and must be serialised
+ * by the caller.
+ * Errors: as mp_grad_norm, and MP_ERR_WORKSPACE if the device would need more
+ * than 4096 partials (a GPU with more than 512 SMs; a 152-SM GB300 needs at
+ * most 1216).
+ * ------------------------------------------------------------------------- */
+int mp_grad_norm_noalloc(const uint16_t* grads, uint64_t n, float clip,
+                         float* d_norm, float* d_scale, double* d_sumsq,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,8 @@ def _load():
     L.mp_stochastic_round.argtypes = [vp, vp, u64, u64, u32, vp]
     L.mp_noise_u32.restype = ctypes.c_int
     L.mp_noise_u32.argtypes = [vp, u64, u64, u32, vp]
+    L.mp_grad_norm_noalloc.restype = ctypes.c_int
+    L.mp_grad_norm_noalloc.argtypes = [vp, u64, f32, vp, vp, vp, vp]
     return L
 
 
@@ -160,6 +162,19 @@ def mp_grad_norm(grads: torch.Tensor, clip: float, workspace: torch.Tensor, d_no
     _check(st, "mp_grad_norm")
 
 
+def mp_grad_norm_noalloc(grads: torch.Tensor, clip: float, d_norm: torch.Tensor, d_scale: torch.Tensor,
+                         d_sumsq: Optional[torch.Tensor] = None, n: Optional[int] = None, stream=None) -> None:
+    """mp_grad_norm for callers that cannot allocate device memory: no
+    workspace; the partial sums live in a small scratch array inside the
+    library. Calls that overlap on one GPU race on that scratch."""
+    n = grads.numel() if n is None else n
+    st = _lib.mp_grad_norm_noalloc(
+        _ptr(grads, _BF16_LIKE, "grads", n), n, clip, _ptr(d_norm, (torch.float32,), "d_norm", 1),
+        _ptr(d_scale, (torch.float32,), "d_scale", 1), _ptr(d_sumsq, (torch.float64,), "d_sumsq", 1),
+        _stream(stream))
+    _check(st, "mp_grad_norm_noalloc")
+
+
 def mp_adamw_step(params: torch.Tensor, grads: torch.Tensor, master: Optional[torch.Tensor],
                   m: torch.Tensor, v: torch.Tensor, table: TensorTable, *, lr: float, beta1: float,
                   beta2: float, eps: float, weight_decay: float, d_grad_scale: Optional[torch.Tensor],
@@ -229,6 +244,6 @@ class Optimizer:
 
 __all__ = [
     "MpError", "MpTensor", "TensorTable", "Optimizer", "lib", "abi_version", "status_string",
-    "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_adamw_step",
+    "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc", "mp_adamw_step",
     "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",
 ]

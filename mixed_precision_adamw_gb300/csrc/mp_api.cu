@@ -41,6 +41,8 @@ cudaError_t device_info(DeviceInfo* out) {
   return cudaSuccess;
 }
 
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 }  // namespace mpk
 
 extern "C" {

@@ -37,6 +37,9 @@ struct DeviceInfo {
 
 cudaError_t device_info(DeviceInfo* out);
 
+// Stores e as this thread's mp_last_cuda_error() and returns MP_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 // seg_end[s] = global index one past segment s; seg_end[nseg-1] == goff + n.
 cudaError_t launch_adamw(const StepArgs& a, const uint64_t* seg_end, bool vec,
                          const DeviceInfo& dev, cudaStream_t stream);

@@ -18,6 +18,7 @@
 #include <cfloat>
 #include <cmath>
 
+#include "mp_adamw.h"
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -157,3 +158,63 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
 }
 
 }  // namespace mpk
+
+// ---------------------------------------------------------------------------
+// mp_grad_norm_noalloc: the same two kernels, with the per-block partial sums
+// kept in a scratch array that this library defines itself, so the caller
+// passes no workspace and nothing is allocated on any call.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Room for 4096 fp64 partials (32 KB). Every GPU that loads the library keeps
+// this array until the process exits. A call needs one slot per norm block:
+// at most 8 x SMs (1216 on a 152-SM GB300).
+constexpr int kNoAllocMaxPartials = 4096;
+static __device__ __align__(256) double g_norm_scratch[kNoAllocMaxPartials];
+
+// Device address of g_norm_scratch, looked up once per device (with that
+// device current) on the first call made on it. In host code the array's name
+// is only a host-side stand-in, never a device address, so it is not passed
+// to a kernel directly.
+void* g_scratch_addr[64];
+
+cudaError_t scratch_address(int device, double** out) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  void* p = g_scratch_addr[device];
+  if (p == nullptr) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_norm_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[device] = p;  // racing first calls store the same address
+  }
+  *out = static_cast<double*>(p);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+// For callers that cannot allocate device memory (a framework that owns all
+// of it and passes in only the tensors, or a loop that must not take the
+// device-wide synchronisation of cudaMalloc/cudaFree): the caller passes the
+// inputs and outputs, and the partial sums go to g_norm_scratch. No call
+// allocates anything. Overlapping calls on one device race on the scratch.
+extern "C" int mp_grad_norm_noalloc(const uint16_t* grads, uint64_t n, float clip, float* d_norm,
+                                    float* d_scale, double* d_sumsq, void* stream) {
+  if ((n != 0 && grads == nullptr) || d_norm == nullptr || d_scale == nullptr) return MP_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(grads) % 2 || reinterpret_cast<uintptr_t>(d_norm) % 4 ||
+      reinterpret_cast<uintptr_t>(d_scale) % 4 || reinterpret_cast<uintptr_t>(d_sumsq) % 8)
+    return MP_ERR_ALIGN;
+  if (!(clip > 0.0f) || !isfinite(clip) || n > (1ull << 62)) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return mpk::record_cuda_error(e);
+  const bool vec = reinterpret_cast<uintptr_t>(grads) % 16 == 0;
+  const int nb = mpk::norm_blocks(n, vec, dev);
+  if (nb > kNoAllocMaxPartials) return MP_ERR_WORKSPACE;  // a GPU with more than 512 SMs
+  double* scratch = nullptr;
+  e = scratch_address(dev.device, &scratch);
+  if (e == cudaSuccess)
+    e = mpk::launch_norm(grads, n, vec, scratch, nb, clip, d_norm, d_scale, d_sumsq,
+                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return mpk::record_cuda_error(e);
+  return MP_OK;
+}
