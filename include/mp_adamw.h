@@ -222,8 +222,8 @@ int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n,
  * or from two threads without ordering — race on it and must be serialised
  * by the caller.
  * Errors: as mp_grad_norm, and MP_ERR_WORKSPACE if the device would need more
- * than 4096 partials (a GPU with more than 512 SMs; a 152-SM GB300 needs at
- * most 1216).
+ * than 4096 partials (a GPU with more than 1024 SMs; a 152-SM GB300 needs at
+ * most 608).
  * ------------------------------------------------------------------------- */
 int mp_grad_norm_noalloc(const uint16_t* grads, uint64_t n, float clip,
                          float* d_norm, float* d_scale, double* d_sumsq,

@@ -19,6 +19,18 @@ constexpr int kThreads = 256;          // threads per block in every kernel
 constexpr int kGroup = 4;              // consecutive elements per fp32 16-B vector
 constexpr int kTile = kThreads * kGroup * 2;  // elements per block-iteration (two groups per thread)
 
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel is launched with programmatic stream serialisation allowed, so
+// the GPU may schedule it while the previous kernel in the stream is still
+// finishing. griddepcontrol.wait blocks until that previous grid has completed
+// and its memory writes are visible; it comes before any global memory access.
+// launch_dependents then lets the next kernel in the stream be scheduled early
+// (it, too, waits before touching memory).
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- rounding randomness ---------------------------------------------------
 // SquirrelNoise5 (Squirrel Eiserloh's published counter-based noise hash) in
 // its 2D form, evaluated at x = low word, y = high word of the 64-bit global

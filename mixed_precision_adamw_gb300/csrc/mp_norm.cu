@@ -25,7 +25,7 @@
 namespace mpk {
 namespace {
 
-constexpr int kNormBlocksPerSm = 8;  // 8 x 256 threads = a full SM
+constexpr int kNormBlocksPerSm = 4;  // 4 x 256 threads per SM, 16 B x 4 in flight each
 constexpr int kUnroll = 4;           // 16-B loads in flight per thread
 
 __device__ __forceinline__ float sumsq8(uint4 w) {
@@ -82,6 +82,7 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
 __global__ void __launch_bounds__(kThreads)
 norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, double* __restrict__ partials) {
   __shared__ double sh[kThreads / 32 + 1];
+  pdl_enter();
   const uint4* g4 = reinterpret_cast<const uint4*>(grads);
   const uint64_t nvec = vec ? n / 8 : 0;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(kThreads)
 norm_finalize_kernel(const double* __restrict__ partials, int nb, float clip,
                      float* d_norm, float* d_scale, double* d_sumsq) {
   __shared__ double sh[kThreads / 32 + 1];
+  pdl_enter();
   double d = 0.0;
   for (int i = threadIdx.x; i < nb; i += kThreads) d = __dadd_rn(d, partials[i]);
   const double S = block_sum(d, sh);
@@ -150,11 +152,11 @@ int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev) {
 
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials, int nblocks,
                         float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream) {
-  norm_partial_kernel<<<nblocks, kThreads, 0, stream>>>(grads, n, vec ? 1 : 0, partials);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(norm_partial_kernel, static_cast<unsigned>(nblocks), kThreads, stream, grads, n,
+                             vec ? 1 : 0, partials);
   if (e != cudaSuccess) return e;
-  norm_finalize_kernel<<<1, kThreads, 0, stream>>>(partials, nblocks, clip, d_norm, d_scale, d_sumsq);
-  return cudaGetLastError();
+  return launch_pdl(norm_finalize_kernel, 1u, kThreads, stream, static_cast<const double*>(partials), nblocks,
+                    clip, d_norm, d_scale, d_sumsq);
 }
 
 }  // namespace mpk
@@ -168,7 +170,7 @@ namespace {
 
 // Room for 4096 fp64 partials (32 KB). Every GPU that loads the library keeps
 // this array until the process exits. A call needs one slot per norm block:
-// at most 8 x SMs (1216 on a 152-SM GB300).
+// at most 4 x SMs (608 on a 152-SM GB300).
 constexpr int kNoAllocMaxPartials = 4096;
 static __device__ __align__(256) double g_norm_scratch[kNoAllocMaxPartials];
 
@@ -209,7 +211,7 @@ extern "C" int mp_grad_norm_noalloc(const uint16_t* grads, uint64_t n, float cli
   if (e != cudaSuccess) return mpk::record_cuda_error(e);
   const bool vec = reinterpret_cast<uintptr_t>(grads) % 16 == 0;
   const int nb = mpk::norm_blocks(n, vec, dev);
-  if (nb > kNoAllocMaxPartials) return MP_ERR_WORKSPACE;  // a GPU with more than 512 SMs
+  if (nb > kNoAllocMaxPartials) return MP_ERR_WORKSPACE;  // a GPU with more than 1024 SMs
   double* scratch = nullptr;
   e = scratch_address(dev.device, &scratch);
   if (e == cudaSuccess)

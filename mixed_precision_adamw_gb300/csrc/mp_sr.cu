@@ -18,6 +18,7 @@ constexpr int kSrBlocksPerSm = 8;
 // thread t converts the 4-element groups at tile offsets 4t and 4t + 1024.
 __global__ void __launch_bounds__(kThreads)
 sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n, uint32_t seed) {
+  pdl_enter();
   const uint64_t ntiles = n / kTile;
   for (uint64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const uint64_t e0 = tile * kTile + threadIdx.x * kGroup;
@@ -40,6 +41,7 @@ sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t
 
 __global__ void __launch_bounds__(kThreads)
 sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n, uint32_t seed) {
+  pdl_enter();
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
     out[i] = static_cast<uint16_t>(sr_bf16(in[i], noise_u32(goff + i, seed) & 0xFFFFu));
@@ -47,6 +49,7 @@ sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint6
 
 __global__ void __launch_bounds__(kThreads)
 noise_kernel(uint32_t* __restrict__ out, uint64_t first, uint64_t n, uint32_t seed) {
+  pdl_enter();
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
     out[i] = noise_u32(first + i, seed);
@@ -67,17 +70,14 @@ cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
   if (vec) {
     const uint64_t ntiles = n / kTile;
     const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);
-    sr_vec_kernel<<<blocks, kThreads, 0, stream>>>(out, in, goff, n, seed);
-  } else {
-    sr_scalar_kernel<<<grid_for(n, dev), kThreads, 0, stream>>>(out, in, goff, n, seed);
+    return launch_pdl(sr_vec_kernel, blocks, kThreads, stream, out, in, goff, n, seed);
   }
-  return cudaGetLastError();
+  return launch_pdl(sr_scalar_kernel, grid_for(n, dev), kThreads, stream, out, in, goff, n, seed);
 }
 
 cudaError_t launch_noise(uint32_t* out, uint64_t first, uint64_t n, uint32_t seed, const DeviceInfo& dev,
                          cudaStream_t stream) {
-  noise_kernel<<<grid_for(n, dev), kThreads, 0, stream>>>(out, first, n, seed);
-  return cudaGetLastError();
+  return launch_pdl(noise_kernel, grid_for(n, dev), kThreads, stream, out, first, n, seed);
 }
 
 }  // namespace mpk

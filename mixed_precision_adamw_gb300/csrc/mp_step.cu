@@ -123,6 +123,7 @@ __device__ __forceinline__ bool read_scale(const StepArgs& p, float& scale) {
 template <bool kMaster, uint32_t CAP>
 __global__ void __launch_bounds__(kThreads)
 adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ SegTable<CAP> segs) {
+  pdl_enter();
   float scale;
   if (!read_scale(p, scale)) return;
   const Hyper h = hyper_of(p);
@@ -183,6 +184,7 @@ adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Seg
 template <bool kMaster, uint32_t CAP>
 __global__ void __launch_bounds__(kThreads)
 adamw_scalar_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ SegTable<CAP> segs) {
+  pdl_enter();
   float scale;
   if (!read_scale(p, scale)) return;
   const Hyper h = hyper_of(p);
@@ -219,16 +221,15 @@ cudaError_t launch_cap(const StepArgs& a, const uint64_t* seg_end, bool vec, con
     uint64_t blocks = ntiles ? ntiles : (a.n + kThreads - 1) / kThreads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, t);
+    return launch_pdl(k, static_cast<unsigned>(blocks), kThreads, stream, a, t);
   } else {
     auto k = adamw_scalar_kernel<kMaster, CAP>;
     const uint64_t cap = static_cast<uint64_t>(dev.sms) * blocks_per_sm(k, dev.device);
     uint64_t blocks = (a.n + kThreads - 1) / kThreads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, t);
+    return launch_pdl(k, static_cast<unsigned>(blocks), kThreads, stream, a, t);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace
