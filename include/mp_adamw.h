@@ -65,7 +65,8 @@ typedef enum mp_status {
     MP_ERR_RANGE = 4,     /* a size, step or hyperparameter is out of range      */
     MP_ERR_NONFINITE = 5, /* device-reported: the clip scale was NaN or Inf      */
     MP_ERR_CUDA = 6,      /* a CUDA runtime call failed (see mp_last_cuda_error) */
-    MP_ERR_WORKSPACE = 7  /* workspace missing or smaller than required          */
+    MP_ERR_WORKSPACE = 7, /* workspace missing or smaller than required          */
+    MP_SKIPPED_OUTLIER = 8 /* device-reported: the outlier check skipped the step */
 } mp_status_t;
 
 /* ABI version this library was built with (MP_ABI_VERSION). */
@@ -150,11 +151,13 @@ int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip,
  *   lr, beta1, beta2, eps, weight_decay   finite; beta1, beta2 in [0, 1).
  *   d_grad_scale  float[1], device (normally mp_grad_norm's d_scale); NULL
  *               means scale 1. If it holds NaN or Inf the kernel writes no
- *               buffer at all and stores MP_ERR_NONFINITE into *d_status.
+ *               buffer at all and stores MP_ERR_NONFINITE into *d_status
+ *               unless *d_status already holds an error (the first wins).
  *   t           1-based step count (t >= 1).
  *   seed        per-step rounding seed.
  *   d_status    int32[1], device, may be NULL; written only on that device-
- *               side error (the caller zeroes it and reads it after a sync).
+ *               side error, and only while it holds 0 (the caller zeroes it
+ *               and reads it after a sync).
  * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_TABLE, MP_ERR_RANGE, MP_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
@@ -199,6 +202,38 @@ int mp_stochastic_round(uint16_t* out, const float* in,
  * ------------------------------------------------------------------------- */
 int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n,
                  uint32_t seed, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Grad-norm outlier check — [LLMC] §4: the train step keeps a window of 128
+ * past grad norms and skips the update when the new norm's z-score is above
+ * a threshold. This runs on the device between mp_grad_norm and
+ * mp_adamw_step (one single-thread kernel, no host round trip):
+ *
+ *   z = (norm - mean(W)) / std(W)   W = the 128 most recent finite norms,
+ *                                   population std, fp64, sums in slot order
+ *   z = NaN while fewer than 128 finite norms have been seen
+ *   if z_threshold > 0 and z > z_threshold:
+ *       *d_scale = NaN                 (so mp_adamw_step writes nothing)
+ *       *d_status = MP_SKIPPED_OUTLIER (if it was 0: the first error wins)
+ *   then a finite norm joins W, replacing the oldest; a non-finite one does not.
+ *
+ *   d_state     device buffer of mp_outlier_state_bytes() bytes, 8-B aligned,
+ *               zeroed once by mp_outlier_reset (or by the caller) before the
+ *               first check; owned by the caller; one per training run.
+ *   d_norm      float[1], device, read (mp_grad_norm's d_norm).
+ *   z_threshold <= 0 or NaN: never skip (z is still computed).
+ *   d_scale     float[1], device, read and possibly set to NaN.
+ *   d_z         double[1], device, written; may be NULL.
+ *   d_status    int32[1], device, may be NULL.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t mp_outlier_state_bytes(void);
+
+int mp_outlier_reset(void* d_state, void* stream);
+
+int mp_outlier_check(void* d_state, const float* d_norm, float z_threshold,
+                     float* d_scale, double* d_z, int32_t* d_status,
+                     void* stream);
 
 /* ---------------------------------------------------------------------------
  * Gradient norm without a workspace. The pages have no counterpart to this

@@ -28,6 +28,7 @@ MP_ERR_RANGE = 4
 MP_ERR_NONFINITE = 5
 MP_ERR_CUDA = 6
 MP_ERR_WORKSPACE = 7
+MP_SKIPPED_OUTLIER = 8
 
 
 class MpError(RuntimeError):
@@ -66,6 +67,12 @@ def _load():
     L.mp_stochastic_round.argtypes = [vp, vp, u64, u64, u32, vp]
     L.mp_noise_u32.restype = ctypes.c_int
     L.mp_noise_u32.argtypes = [vp, u64, u64, u32, vp]
+    L.mp_outlier_state_bytes.restype = ctypes.c_size_t
+    L.mp_outlier_state_bytes.argtypes = []
+    L.mp_outlier_reset.restype = ctypes.c_int
+    L.mp_outlier_reset.argtypes = [vp, vp]
+    L.mp_outlier_check.restype = ctypes.c_int
+    L.mp_outlier_check.argtypes = [vp, vp, f32, vp, vp, vp, vp]
     L.mp_grad_norm_noalloc.restype = ctypes.c_int
     L.mp_grad_norm_noalloc.argtypes = [vp, u64, f32, vp, vp, vp, vp]
     return L
@@ -208,6 +215,41 @@ def mp_noise_u32(out: torch.Tensor, first_index: int, seed: int, n: Optional[int
     _check(st, "mp_noise_u32")
 
 
+def mp_outlier_state_bytes() -> int:
+    return int(_lib.mp_outlier_state_bytes())
+
+
+def mp_outlier_reset(d_state: torch.Tensor, stream=None) -> None:
+    _check(_lib.mp_outlier_reset(_ptr(d_state, (torch.uint8, torch.float64), "d_state", None), _stream(stream)),
+           "mp_outlier_reset")
+
+
+def mp_outlier_check(d_state: torch.Tensor, d_norm: torch.Tensor, z_threshold: float, d_scale: torch.Tensor,
+                     d_z: Optional[torch.Tensor] = None, d_status: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    """Enqueue the grad-norm z-score check; a skip sets *d_scale to NaN."""
+    if d_state.numel() * d_state.element_size() < mp_outlier_state_bytes():
+        raise ValueError("d_state: smaller than mp_outlier_state_bytes()")
+    st = _lib.mp_outlier_check(
+        _ptr(d_state, (torch.uint8, torch.float64), "d_state"), _ptr(d_norm, (torch.float32,), "d_norm", 1),
+        z_threshold, _ptr(d_scale, (torch.float32,), "d_scale", 1), _ptr(d_z, (torch.float64,), "d_z", 1),
+        _ptr(d_status, (torch.int32,), "d_status", 1), _stream(stream))
+    _check(st, "mp_outlier_check")
+
+
+class OutlierDetector:
+    """Device state of the grad-norm outlier check (window of 128 norms)."""
+
+    def __init__(self, z_threshold: float, device=None):
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.z_threshold = float(z_threshold)
+        self.state = torch.zeros(mp_outlier_state_bytes(), dtype=torch.uint8, device=dev)
+        self.d_z = torch.full((1,), float("nan"), dtype=torch.float64, device=dev)
+
+    def check(self, d_norm, d_scale, d_status=None, stream=None):
+        mp_outlier_check(self.state, d_norm, self.z_threshold, d_scale, self.d_z, d_status, stream=stream)
+
+
 class Optimizer:
     """Convenience wrapper holding the device state of one optimizer step:
     workspace, norm/scale/status scalars and the packed tensor table.
@@ -218,7 +260,8 @@ class Optimizer:
     """
 
     def __init__(self, table_entries: Sequence[Tuple[int, int, int]], *, lr: float, beta1: float,
-                 beta2: float, eps: float, weight_decay: float, clip: float, device=None):
+                 beta2: float, eps: float, weight_decay: float, clip: float, device=None,
+                 outlier_z: Optional[float] = None):
         self.table = TensorTable(table_entries)
         self.n = self.table.total
         self.hyper = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
@@ -229,21 +272,32 @@ class Optimizer:
         self.d_norm = torch.zeros(1, dtype=torch.float32, device=dev)
         self.d_scale = torch.zeros(1, dtype=torch.float32, device=dev)
         self.d_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.outlier = OutlierDetector(outlier_z, device=dev) if outlier_z is not None else None
 
     def step(self, params, grads, master, m, v, t: int, seed: int, stream=None):
         mp_grad_norm(grads, self.clip, self.workspace, self.d_norm, self.d_scale, n=self.n, stream=stream)
+        if self.outlier is not None:
+            self.outlier.check(self.d_norm, self.d_scale, self.d_status, stream=stream)
         mp_adamw_step(params, grads, master, m, v, self.table, d_grad_scale=self.d_scale, t=t, seed=seed,
                       d_status=self.d_status, n=self.n, stream=stream, **self.hyper)
 
-    def check_status(self) -> None:
+    def take_status(self) -> int:
+        """Device status of the steps since the last call (0, MP_ERR_NONFINITE
+        or MP_SKIPPED_OUTLIER; the first one recorded wins); clears it."""
         st = int(self.d_status.item())
         if st != MP_OK:
             self.d_status.zero_()
+        return st
+
+    def check_status(self) -> None:
+        st = self.take_status()
+        if st != MP_OK:
             raise MpError(st, "mp_adamw_step (device)")
 
 
 __all__ = [
-    "MpError", "MpTensor", "TensorTable", "Optimizer", "lib", "abi_version", "status_string",
+    "MpError", "MpTensor", "TensorTable", "Optimizer", "OutlierDetector", "mp_outlier_state_bytes",
+    "mp_outlier_reset", "mp_outlier_check", "lib", "abi_version", "status_string",
     "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc", "mp_adamw_step",
     "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",
 ]

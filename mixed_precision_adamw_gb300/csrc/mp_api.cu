@@ -59,6 +59,7 @@ const char* mp_status_string(int status) {
     case MP_ERR_NONFINITE: return "MP_ERR_NONFINITE: the clip scale was NaN or Inf; nothing was written";
     case MP_ERR_CUDA: return "MP_ERR_CUDA: a CUDA runtime call failed";
     case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE: workspace missing or too small";
+    case MP_SKIPPED_OUTLIER: return "MP_SKIPPED_OUTLIER: the grad-norm z-score was above the threshold; step skipped";
     default: return "unknown mp_status";
   }
 }

@@ -110,7 +110,8 @@ __device__ __forceinline__ void elem_update(const StepArgs& p, const SegTable<CA
 __device__ __forceinline__ bool read_scale(const StepArgs& p, float& scale) {
   scale = (p.d_scale != nullptr) ? *p.d_scale : 1.0f;
   if (!isfinite(scale)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0 && p.d_status != nullptr) *p.d_status = 5;  // MP_ERR_NONFINITE
+    // MP_ERR_NONFINITE, unless an earlier error (e.g. an outlier skip) is already recorded
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.d_status != nullptr) atomicCAS(p.d_status, 0, 5);
     return false;
   }
   return true;

@@ -22,6 +22,13 @@ class OracleTensor(ctypes.Structure):
                 ("decay", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
+OUTLIER_WINDOW = 128
+
+
+class OracleOutlier(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_double * OUTLIER_WINDOW), ("count", ctypes.c_uint64)]
+
+
 _lib = None
 
 
@@ -58,6 +65,9 @@ def lib():
             ctypes.POINTER(OracleTensor), ctypes.c_int32,
             ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
             ctypes.c_float, ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
+        L.oracle_outlier_check.restype = ctypes.c_int
+        L.oracle_outlier_check.argtypes = [ctypes.POINTER(OracleOutlier), ctypes.c_float, ctypes.c_float,
+                                           _c_f32p, _c_f64p]
         _lib = L
     return _lib
 
@@ -149,3 +159,18 @@ def adamw_step(params, grads, master, m, v, global_offset, table_entries,
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Exact widening of raw bf16 patterns (test-side convenience)."""
     return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+class OutlierCheck:
+    """Stateful wrapper of oracle_outlier_check (window of 128 finite norms)."""
+
+    def __init__(self):
+        self.state = OracleOutlier()
+
+    def check(self, norm: float, z_threshold: float, scale: float):
+        """Returns (status, z, scale_after)."""
+        sc = ctypes.c_float(scale)
+        z = ctypes.c_double()
+        st = lib().oracle_outlier_check(ctypes.byref(self.state), norm, z_threshold, ctypes.byref(sc),
+                                        ctypes.byref(z))
+        return int(st), z.value, sc.value

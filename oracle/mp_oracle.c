@@ -213,3 +213,43 @@ int oracle_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
     }
     return 0;
 }
+
+/* ---- Outlier skip --------------------------------------------------------
+ * [LLMC] §4: before the update, the train step feeds the grad norm to an
+ * outlier detector holding a window of 128 past values; if the norm's
+ * z-score is above a threshold the update is skipped. Reading taken here:
+ * z = (x - mean) / std over the 128 most recent finite norms (population
+ * standard deviation, both sums in array-slot order), z is NaN while fewer
+ * than 128 norms have been seen, the check happens before x joins the
+ * window, a threshold <= 0 never skips, and a non-finite norm never enters
+ * the window (the step is refused for it anyway). */
+int oracle_outlier_check(oracle_outlier* st, float norm, float z_threshold,
+                         float* scale, double* z)
+{
+    const double x = (double)norm;
+    double zz = NAN;
+    if (st->count >= ORACLE_OUTLIER_WINDOW) {
+        double sum = 0.0;
+        for (int i = 0; i < ORACLE_OUTLIER_WINDOW; ++i)
+            sum += st->window[i];
+        const double mean = sum / ORACLE_OUTLIER_WINDOW;
+        double ss = 0.0;
+        for (int i = 0; i < ORACLE_OUTLIER_WINDOW; ++i) {
+            const double d = st->window[i] - mean;
+            ss += d * d;
+        }
+        const double sd = sqrt(ss / ORACLE_OUTLIER_WINDOW);
+        zz = (x - mean) / sd;
+    }
+    *z = zz;
+    int status = 0;
+    if (z_threshold > 0.0f && zz > (double)z_threshold) {
+        *scale = NAN;
+        status = 8;
+    }
+    if (isfinite(x)) {
+        st->window[st->count % ORACLE_OUTLIER_WINDOW] = x;
+        st->count += 1;
+    }
+    return status;
+}

@@ -70,6 +70,19 @@ int oracle_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
                       float weight_decay, float scale,
                       int32_t t, uint32_t seed);
 
+/* Grad-norm outlier check: window of the last 128 finite norms. */
+#define ORACLE_OUTLIER_WINDOW 128
+typedef struct oracle_outlier {
+    double window[ORACLE_OUTLIER_WINDOW];
+    uint64_t count; /* finite norms pushed so far */
+} oracle_outlier;
+
+/* z-score of `norm` against the window (NaN until it holds 128 norms); if z
+ * exceeds a positive threshold, *scale becomes NaN and 8 is returned (skip),
+ * else 0. A finite norm then enters the window, replacing the oldest. */
+int oracle_outlier_check(oracle_outlier* st, float norm, float z_threshold,
+                         float* scale, double* z);
+
 #ifdef __cplusplus
 }
 #endif

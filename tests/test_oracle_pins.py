@@ -503,3 +503,56 @@ def test_resume_rebuilds_bf16_bit_identically():
     run(b, 4, 7)
     for k in a:
         assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+
+
+# --------------------------------------------------------------------------
+# Outlier skip — llm.c ch. 04 §4: a window of 128 past grad norms, z-score of
+# the new norm, skip the update when z is above a threshold.
+# --------------------------------------------------------------------------
+def test_outlier_zscore_matches_statistics_pstdev():
+    import statistics
+    rng = np.random.default_rng(7)
+    o = oracle.OutlierCheck()
+    hist = []
+    for i in range(400):
+        x = float(np.float32(1.0 + 0.1 * rng.standard_normal() + (5.0 if i % 97 == 96 else 0.0)))
+        st, z, sc = o.check(x, 0.0, 0.5)
+        assert st == 0 and sc == np.float32(0.5)  # threshold 0 never skips
+        if len(hist) < 128:
+            assert math.isnan(z)
+        else:
+            w = hist[-128:]
+            ref = (x - statistics.fmean(w)) / statistics.pstdev(w)
+            assert abs(z - ref) <= 1e-9 * max(1.0, abs(ref))
+        hist.append(x)
+
+
+def test_outlier_closed_form_and_skip():
+    o = oracle.OutlierCheck()
+    m, d = 2.0, 0.25  # window: 64 x (m - d) and 64 x (m + d): mean m, population std d
+    for i in range(128):
+        o.check(m - d if i % 2 else m + d, 3.0, 1.0)
+    st, z, sc = o.check(m + 3 * d, 2.5, 0.75)
+    assert z == 3.0 and st == 8 and math.isnan(sc)  # z > 2.5: skipped, scale poisoned
+    o2 = oracle.OutlierCheck()
+    for i in range(128):
+        o2.check(m - d if i % 2 else m + d, 3.0, 1.0)
+    st, z, sc = o2.check(m + 3 * d, 3.0, 0.75)
+    assert z == 3.0 and st == 0 and sc == np.float32(0.75)  # not above the threshold: kept
+
+
+def test_outlier_window_ignores_nonfinite_norms_and_slides():
+    o = oracle.OutlierCheck()
+    for i in range(127):
+        o.check(1.0, 3.0, 1.0)
+    for bad in (float("nan"), float("inf")):
+        st, z, _ = o.check(bad, 3.0, 1.0)
+        assert math.isnan(z) and o.state.count == 127
+    o.check(1.0, 3.0, 1.0)
+    assert o.state.count == 128
+    st, z, _ = o.check(1.0, 3.0, 1.0)
+    assert math.isnan(z)  # zero spread: 0 / 0
+    st, z, _ = o.check(2.0, 3.0, 1.0)
+    assert z == math.inf and st == 8
+    # the window now holds 127 ones and one 2.0 (the oldest slot was replaced)
+    assert sorted(o.state.window)[-1] == 2.0 and sum(o.state.window) == 129.0
