@@ -42,7 +42,13 @@ import workloads as W  # noqa: E402
 
 METRIC = "AdamW+SR step: Gparams/s and HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "Gparams/s"
-WORKLOAD = "gpt2_124m"
+WORKLOAD = "gpt2_124m"  # the default line; --workload picks the other parameter sets
+WORKLOAD_NAMES = {
+    "tiny": "tiny GPT-style parameter set (d 32, 2 layers, 28,672 params)",
+    "gpt2_124m": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
+    "gpt2_1558m": "GPT-2 1.5B parameter set (V 50304, T 1024, d 1600, 48 layers, tied wte)",
+    "llama3_8b": "Llama-3-8B parameter set (d 4096, 32 layers, GQA 32/8, SwiGLU 14336, V 128256 untied)",
+}
 STEP_BYTES_MASTER = 28   # 2 grad + 3x4 (master, m, v) read; 3x4 + 2 (param) written
 STEP_BYTES_NOMASTER = 22
 NORM_BYTES = 2
@@ -184,13 +190,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
     H = W.HYPER
-    entries = W.layout(W.specs_for(WORKLOAD))
+    workload = args.workload
+    entries = W.layout(W.specs_for(workload))
     if args.params:
         entries = prefix_entries(entries, args.params)
     tab = W.table(entries)
     N = W.total(entries)
-    st = W.make_state(WORKLOAD, device=device, entries=entries)
-    grads = [W.make_grads(WORKLOAD, s, device=device, entries=entries) for s in (1, 2)]
+    st = W.make_state(workload, device=device, entries=entries)
+    grads = [W.make_grads(workload, s, device=device, entries=entries) for s in (1, 2)]
     opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
                        weight_decay=H["weight_decay"], clip=H["clip"], device=device)
     stream = torch.cuda.current_stream(device)
@@ -240,7 +247,7 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = measured_hbm_peak()
     achieved = STEP_BYTES_MASTER * N / (step_kernel_ms / 1e3) / 1e9
-    traffic = profiled_traffic_bytes()
+    traffic = profiled_traffic_bytes() if workload == WORKLOAD else None
     roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master>", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": traffic, "algorithmic_bytes_per_launch": STEP_BYTES_MASTER * N,
@@ -259,10 +266,12 @@ def run_ours(args, world, rank, local):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
+        "config": {"workload": WORKLOAD_NAMES[workload],
                    "params": N, "tensors": len(entries), "variant": "fp32 master + bf16 params, clip 1.0",
                    "bytes_per_param": STEP_BYTES_MASTER + NORM_BYTES,
-                   "l2": "no flush: 3.7 GB touched per step, > 129 MB L2",
+                   "l2": (f"no flush: {(STEP_BYTES_MASTER + NORM_BYTES) * N / 1e9:.2f} GB touched per step, > 129 MB L2"
+                          if (STEP_BYTES_MASTER + NORM_BYTES) * N > 4 * 129e6 else
+                          "working set L2-resident (launch-bound latency case)"),
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "hbm_gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N * args.steps / (total_ms / 1e3) / 1e9, 1),
         "hbm_frac_of_measured": round((STEP_BYTES_MASTER + NORM_BYTES) * N * args.steps / (total_ms / 1e3)
@@ -299,17 +308,15 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
                                              stream=stream), iters, stream)
     out["grad_norm"] = {"ms": round(ms, 5), "gbs": round(NORM_BYTES * N / ms / 1e6, 1),
                         "frac": round(NORM_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_param": NORM_BYTES}
-    # no-master variant on its own state (params, m, v)
-    p2 = st["params"].clone()
-    m2 = st["m"].clone()
-    v2 = st["v"].clone()
-    ms = time_events(lambda: mp.mp_adamw_step(p2, g, None, m2, v2, opt.table, d_grad_scale=opt.d_scale, t=5,
-                                              seed=5, n=N, stream=stream, **kw), iters, stream)
+    # no-master variant, in place on params, m, v (no extra copy: the
+    # Llama-3-8B state alone is 128 GB)
+    ms = time_events(lambda: mp.mp_adamw_step(st["params"], g, None, st["m"], st["v"], opt.table,
+                                              d_grad_scale=opt.d_scale, t=5, seed=5, n=N, stream=stream, **kw),
+                     iters, stream)
     out["step_no_master"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
                              "gbs": round(STEP_BYTES_NOMASTER * N / ms / 1e6, 1),
                              "frac": round(STEP_BYTES_NOMASTER * N / ms / 1e6 / peak, 4),
                              "bytes_per_param": STEP_BYTES_NOMASTER}
-    del p2, m2, v2
     ms = time_events(lambda: mp.mp_stochastic_round(st["params"], st["master"], 7, n=N, stream=stream), iters,
                      stream)
     out["stochastic_round"] = {"ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
@@ -457,6 +464,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_NAMES), default=WORKLOAD,
+                    help="parameter set (default: the GPT-2 124M line)")
     ap.add_argument("--params", type=int, default=0,
                     help="use only the first P params of the set (small cases for profiling)")
     ap.add_argument("--quick", action="store_true",
