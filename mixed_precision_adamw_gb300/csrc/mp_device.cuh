@@ -35,12 +35,16 @@ __device__ __forceinline__ void pdl_enter() {
 // SquirrelNoise5 (Squirrel Eiserloh's published counter-based noise hash) in
 // its 2D form, evaluated at x = low word, y = high word of the 64-bit global
 // element index. A pure function of (index, seed): independent of the grid.
-__device__ __forceinline__ uint32_t noise_u32(uint64_t k, uint32_t seed) {
-  const uint32_t x = static_cast<uint32_t>(k);
-  const uint32_t y = static_cast<uint32_t>(k >> 32);
-  uint32_t h = x + 198491317u * y;
-  h *= 0xD2A80A3Fu;
-  h += seed;
+constexpr uint32_t kNoisePrime = 198491317u;  // folds y into x (the 2D entry)
+
+// 2D fold of a global index into the 1D noise position.
+__device__ __forceinline__ uint32_t noise_pos(uint64_t k) {
+  return static_cast<uint32_t>(k) + kNoisePrime * static_cast<uint32_t>(k >> 32);
+}
+
+// Every SquirrelNoise5 round except the final xor-shift by 17.
+__device__ __forceinline__ uint32_t noise_rounds(uint32_t pos, uint32_t seed) {
+  uint32_t h = pos * 0xD2A80A3Fu + seed;
   h ^= h >> 9;
   h += 0xA884F197u;
   h ^= h >> 11;
@@ -49,19 +53,42 @@ __device__ __forceinline__ uint32_t noise_u32(uint64_t k, uint32_t seed) {
   h += 0xB79F3ABBu;
   h ^= h >> 15;
   h *= 0x1B56C4F5u;
-  h ^= h >> 17;
   return h;
+}
+
+__device__ __forceinline__ uint32_t noise_u32(uint64_t k, uint32_t seed) {
+  const uint32_t h = noise_rounds(noise_pos(k), seed);
+  return h ^ (h >> 17);
+}
+
+// 0xFFFF minus the 16-bit draw (the low half of the noise), i.e. ~draw & 0xFFFF.
+__device__ __forceinline__ uint32_t draw16_complement(uint32_t pos, uint32_t seed) {
+  const uint32_t h = noise_rounds(pos, seed);
+  return ~(h ^ (h >> 17)) & 0xFFFFu;
+}
+
+// Noise positions of the 4 consecutive indices k0 .. k0+3 from one fold:
+// noise_pos(k0 + j) = noise_pos(k0) + j, plus the prime once if the low word
+// wrapped past 2^32 between k0 and k0 + j (the high word then grew by one).
+// Branch-free, so the unrolled update is not duplicated per case.
+__device__ __forceinline__ void noise_pos4(uint64_t k0, uint32_t (&pos)[4]) {
+  const uint32_t lo = static_cast<uint32_t>(k0);
+  const uint32_t p0 = noise_pos(k0);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pos[j] = p0 + j + (lo > 0xFFFFFFFFu - j ? kNoisePrime : 0u);
 }
 
 // ---- stochastic rounding fp32 -> bf16 -------------------------------------
 // Keep the top half of the fp32 pattern and add one (the bf16 neighbour away
-// from zero) when the discarded low half exceeds a uniform 16-bit draw, so
-// the probability of rounding away from zero is lo16 / 65536. NaN becomes
-// the canonical quiet NaN (truncation could otherwise yield an infinity).
-__device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t rand16) {
+// from zero) when the discarded low half exceeds a uniform 16-bit draw r, so
+// the probability of rounding away from zero is lo16 / 65536. With
+// c = 0xFFFF - r, the carry out of lo16 + c is exactly [lo16 > r], so the
+// result is the high half of b + c (no non-NaN pattern overflows: the largest
+// is -Inf, 0xFF800000). NaN becomes the canonical quiet NaN (truncation could
+// otherwise yield an infinity).
+__device__ __forceinline__ uint32_t sr_bf16_c(float x, uint32_t draw_complement) {
   const uint32_t b = __float_as_uint(x);
-  const uint32_t up = (b & 0xFFFFu) > rand16 ? 1u : 0u;
-  const uint32_t r = (b >> 16) + up;
+  const uint32_t r = (b + draw_complement) >> 16;
   return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : r;
 }
 

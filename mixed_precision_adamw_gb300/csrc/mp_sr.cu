@@ -25,18 +25,20 @@ sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t
     const uint64_t e1 = e0 + kThreads * kGroup;
     const float4 a = __ldcs(reinterpret_cast<const float4*>(in + e0));
     const float4 b = __ldcs(reinterpret_cast<const float4*>(in + e1));
-    const uint64_t k0 = goff + e0, k1 = goff + e1;
+    uint32_t pa[kGroup], pb[kGroup];
+    noise_pos4(goff + e0, pa);
+    noise_pos4(goff + e1, pb);
     uint2 qa, qb;
-    qa.x = sr_bf16(a.x, noise_u32(k0 + 0, seed) & 0xFFFFu) | (sr_bf16(a.y, noise_u32(k0 + 1, seed) & 0xFFFFu) << 16);
-    qa.y = sr_bf16(a.z, noise_u32(k0 + 2, seed) & 0xFFFFu) | (sr_bf16(a.w, noise_u32(k0 + 3, seed) & 0xFFFFu) << 16);
-    qb.x = sr_bf16(b.x, noise_u32(k1 + 0, seed) & 0xFFFFu) | (sr_bf16(b.y, noise_u32(k1 + 1, seed) & 0xFFFFu) << 16);
-    qb.y = sr_bf16(b.z, noise_u32(k1 + 2, seed) & 0xFFFFu) | (sr_bf16(b.w, noise_u32(k1 + 3, seed) & 0xFFFFu) << 16);
+    qa.x = sr_bf16_c(a.x, draw16_complement(pa[0], seed)) | (sr_bf16_c(a.y, draw16_complement(pa[1], seed)) << 16);
+    qa.y = sr_bf16_c(a.z, draw16_complement(pa[2], seed)) | (sr_bf16_c(a.w, draw16_complement(pa[3], seed)) << 16);
+    qb.x = sr_bf16_c(b.x, draw16_complement(pb[0], seed)) | (sr_bf16_c(b.y, draw16_complement(pb[1], seed)) << 16);
+    qb.y = sr_bf16_c(b.z, draw16_complement(pb[2], seed)) | (sr_bf16_c(b.w, draw16_complement(pb[3], seed)) << 16);
     __stcs(reinterpret_cast<uint2*>(out + e0), qa);
     __stcs(reinterpret_cast<uint2*>(out + e1), qb);
   }
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t i = ntiles * kTile + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
-    out[i] = static_cast<uint16_t>(sr_bf16(in[i], noise_u32(goff + i, seed) & 0xFFFFu));
+    out[i] = static_cast<uint16_t>(sr_bf16_c(in[i], draw16_complement(noise_pos(goff + i), seed)));
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -44,7 +46,7 @@ sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint6
   pdl_enter();
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
-    out[i] = static_cast<uint16_t>(sr_bf16(in[i], noise_u32(goff + i, seed) & 0xFFFFu));
+    out[i] = static_cast<uint16_t>(sr_bf16_c(in[i], draw16_complement(noise_pos(goff + i), seed)));
 }
 
 __global__ void __launch_bounds__(kThreads)

@@ -79,11 +79,12 @@ __device__ __forceinline__ uint2 group_update(uint2 graw, float4& m4, float4& v4
   const float g[kGroup] = {bf16_lo(graw.x), bf16_hi(graw.x), bf16_lo(graw.y), bf16_hi(graw.y)};
   float mm[kGroup] = {m4.x, m4.y, m4.z, m4.w};
   float vv[kGroup] = {v4.x, v4.y, v4.z, v4.w};
-  uint32_t r[kGroup];
+  uint32_t r[kGroup], pos[kGroup];
+  noise_pos4(gi, pos);
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) {
     w[j] = adamw_update(g[j], mm[j], vv[j], w[j], wd[j], scale, h);
-    r[j] = sr_bf16(w[j], noise_u32(gi + j, seed) & 0xFFFFu);
+    r[j] = sr_bf16_c(w[j], draw16_complement(pos[j], seed));
   }
   m4 = make_float4(mm[0], mm[1], mm[2], mm[3]);
   v4 = make_float4(vv[0], vv[1], vv[2], vv[3]);
@@ -102,7 +103,7 @@ __device__ __forceinline__ void elem_update(const StepArgs& p, const SegTable<CA
   p.m[i] = m;
   p.v[i] = v;
   if (kMaster) p.master[i] = w;
-  p.params[i] = static_cast<uint16_t>(sr_bf16(w, noise_u32(gi, p.seed) & 0xFFFFu));
+  p.params[i] = static_cast<uint16_t>(sr_bf16_c(w, draw16_complement(noise_pos(gi), p.seed)));
 }
 
 // Reads the clip scale; a non-finite scale stops every thread before any

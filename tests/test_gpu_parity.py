@@ -88,7 +88,10 @@ def _special_f32(n, rng):
 
 @pytest.mark.parametrize("n,pad_in,pad_out,goff", [
     (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32),
-    (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000)])
+    (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000),
+    # vector path crossing 2^32 inside a 4-element group (offset not a multiple of 4)
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5001), (2048 * 7 + 5, 0, 0, (1 << 32) - 5002),
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), (2048 * 7 + 5, 0, 0, (3 << 32) - 1)])
 def test_stochastic_round_bit_exact(n, pad_in, pad_out, goff):
     rng = np.random.default_rng(n + pad_in)
     x = _special_f32(n, rng) if n > 2000 else rng.standard_normal(n).astype(np.float32)
@@ -281,6 +284,23 @@ def test_step_random_tables(n, pad, with_master, tmax):
     assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, lr, b1, b2, eps,
                              wd, f32(scale), t, seed) == 0
     _compare(d, host, f"random n={n}")
+
+
+@pytest.mark.parametrize("goff", [(1 << 32) - 3001, (1 << 32) - 3002, (1 << 32) - 3003, (1 << 32) - 3004])
+def test_step_global_offset_across_2_pow_32(goff):
+    """A shard whose global range crosses index 2^32 from an offset that is
+    not a multiple of 4: the rounding draws' 2D fold changes inside a group."""
+    n = 2048 * 5 + 17
+    _, params, grads, master, m, v = _random_case(n, 17)
+    tab = [(0, goff - 1000, 1), (goff - 1000, 2500, 0), (goff + 1500, n, 1)]
+    d = dict(params=dev_u16(params), grads=dev_u16(grads), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master))
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=1e-2,
+                     beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.3, d_grad_scale=None, t=2, seed=77,
+                     global_offset=goff)
+    host = dict(params=params.copy(), master=master.copy(), m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], goff, tab, 1e-2, 0.9,
+                             0.95, 1e-8, 0.3, 1.0, 2, 77) == 0
+    _compare(d, host, f"offset {goff}")
 
 
 def test_step_many_segments_split_into_launches():
