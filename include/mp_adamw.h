@@ -66,8 +66,15 @@ typedef enum mp_status {
     MP_ERR_NONFINITE = 5, /* device-reported: the clip scale was NaN or Inf      */
     MP_ERR_CUDA = 6,      /* a CUDA runtime call failed (see mp_last_cuda_error) */
     MP_ERR_WORKSPACE = 7, /* workspace missing or smaller than required          */
-    MP_SKIPPED_OUTLIER = 8 /* device-reported: the outlier check skipped the step */
+    MP_SKIPPED_OUTLIER = 8, /* device-reported: the outlier check skipped the step */
+    MP_ERR_ACCESS = 9     /* a host buffer is not page-locked memory the device can read */
 } mp_status_t;
+
+/* Optimizer hyperparameters of mp_optimizer_step. */
+typedef struct mp_hyper {
+    float lr, beta1, beta2, eps, weight_decay;
+    float clip; /* clip threshold of the grad norm (the train step uses 1.0) */
+} mp_hyper_t;
 
 /* ABI version this library was built with (MP_ABI_VERSION). */
 int mp_abi_version(void);
@@ -234,6 +241,43 @@ int mp_outlier_reset(void* d_state, void* stream);
 int mp_outlier_check(void* d_state, const float* d_norm, float z_threshold,
                      float* d_scale, double* d_z, int32_t* d_status,
                      void* stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole step in one call — [LLMC] §4's order: grad norm and clip scale,
+ * the optional outlier check, then the AdamW + stochastic-rounding update of
+ * the whole buffer [0, n). Enqueues mp_grad_norm's kernels, mp_outlier_check
+ * (if outlier_state != NULL) and mp_adamw_step's kernel(s); same arguments,
+ * same results as making those calls in that order with global_offset 0.
+ * (A ZeRO-1 shard calls the pieces: its norm must cover every shard.)
+ *
+ *   grads        bf16[n], device. If host_grads is NULL, the gradients to use;
+ *                otherwise it receives the device copy of host_grads.
+ *   host_grads   bf16[n] in page-locked host memory (cudaHostAlloc'd or
+ *                cudaHostRegister'ed), or NULL. The norm kernel reads it over
+ *                the host link and writes `grads` in the same pass, so the
+ *                transfer overlaps the reduction. MP_ERR_ACCESS if the device
+ *                cannot read it.
+ *   hyper        host struct: lr, beta1, beta2, eps, weight_decay, clip.
+ *   workspace    as mp_grad_norm (mp_grad_norm_workspace_bytes(n) bytes).
+ *   outlier_state, outlier_z, d_z   as mp_outlier_check's d_state, z_threshold
+ *                and d_z; outlier_state NULL skips the check.
+ *   d_norm, d_scale   float[1] device outputs (norm and clip scale).
+ *   d_status     int32[1], device, may be NULL (as mp_adamw_step).
+ *   host_norm    float[1] host destination of the norm (copied at the end of
+ *                the stream's work; page-locked for an asynchronous copy), or
+ *                NULL.
+ * All other arguments as mp_adamw_step. Every argument is checked before
+ * anything is enqueued.
+ * Errors: as mp_grad_norm and mp_adamw_step, and MP_ERR_ACCESS.
+ * ------------------------------------------------------------------------- */
+int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads,
+                      float* master, float* m, float* v, uint64_t n,
+                      const mp_tensor_t* table, int32_t n_tensors,
+                      const mp_hyper_t* hyper, int32_t t, uint32_t seed,
+                      void* workspace, size_t workspace_bytes,
+                      void* outlier_state, float outlier_z, double* d_z,
+                      float* d_norm, float* d_scale, int32_t* d_status,
+                      float* host_norm, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Gradient norm without a workspace. The pages have no counterpart to this

@@ -29,6 +29,7 @@ MP_ERR_NONFINITE = 5
 MP_ERR_CUDA = 6
 MP_ERR_WORKSPACE = 7
 MP_SKIPPED_OUTLIER = 8
+MP_ERR_ACCESS = 9
 
 
 class MpError(RuntimeError):
@@ -41,6 +42,11 @@ class MpError(RuntimeError):
 class MpTensor(ctypes.Structure):
     _fields_ = [("offset", ctypes.c_uint64), ("size", ctypes.c_uint64),
                 ("decay", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class MpHyper(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("clip", ctypes.c_float)]
 
 
 def _load():
@@ -73,6 +79,10 @@ def _load():
     L.mp_outlier_reset.argtypes = [vp, vp]
     L.mp_outlier_check.restype = ctypes.c_int
     L.mp_outlier_check.argtypes = [vp, vp, f32, vp, vp, vp, vp]
+    L.mp_optimizer_step.restype = ctypes.c_int
+    L.mp_optimizer_step.argtypes = [vp, vp, vp, vp, vp, vp, u64, ctypes.POINTER(MpTensor), i32,
+                                    ctypes.POINTER(MpHyper), i32, u32, vp, ctypes.c_size_t, vp, f32, vp,
+                                    vp, vp, vp, vp, vp]
     L.mp_grad_norm_noalloc.restype = ctypes.c_int
     L.mp_grad_norm_noalloc.argtypes = [vp, u64, f32, vp, vp, vp, vp]
     return L
@@ -215,6 +225,42 @@ def mp_noise_u32(out: torch.Tensor, first_index: int, seed: int, n: Optional[int
     _check(st, "mp_noise_u32")
 
 
+def _host_ptr(t: Optional[torch.Tensor], dtypes, name: str, n: Optional[int] = None) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name}: must be a host (CPU) tensor")
+    if t.dtype not in dtypes or not t.is_contiguous():
+        raise TypeError(f"{name}: contiguous tensor of {dtypes} expected")
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name}: {t.numel()} elements < {n}")
+    return t.data_ptr()
+
+
+def mp_optimizer_step(params: torch.Tensor, grads: torch.Tensor, master: Optional[torch.Tensor], m: torch.Tensor,
+                      v: torch.Tensor, table: "TensorTable", hyper: MpHyper, *, t: int, seed: int,
+                      workspace: torch.Tensor, d_norm: torch.Tensor, d_scale: torch.Tensor,
+                      d_status: Optional[torch.Tensor] = None, outlier_state: Optional[torch.Tensor] = None,
+                      outlier_z: float = 0.0, d_z: Optional[torch.Tensor] = None,
+                      host_grads: Optional[torch.Tensor] = None,
+                      host_norm: Optional[torch.Tensor] = None, n: Optional[int] = None, stream=None) -> None:
+    """Enqueue the whole step: norm + clip scale, optional outlier check, AdamW + SR.
+    host_grads (pinned CPU bf16) is read by the norm kernel, which fills `grads`."""
+    n = m.numel() if n is None else n
+    st = _lib.mp_optimizer_step(
+        _ptr(params, _BF16_LIKE, "params", n), _ptr(grads, _BF16_LIKE, "grads", n),
+        _host_ptr(host_grads, _BF16_LIKE, "host_grads", n),
+        _ptr(master, (torch.float32,), "master", n), _ptr(m, (torch.float32,), "m", n),
+        _ptr(v, (torch.float32,), "v", n), n, table.ctypes_array, table.n_tensors, ctypes.byref(hyper), t,
+        seed & 0xFFFFFFFF, _ptr(workspace, (torch.uint8, torch.float64, torch.int64), "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _ptr(outlier_state, (torch.uint8, torch.float64), "outlier_state"), outlier_z,
+        _ptr(d_z, (torch.float64,), "d_z", 1), _ptr(d_norm, (torch.float32,), "d_norm", 1), _ptr(d_scale, (torch.float32,), "d_scale", 1),
+        _ptr(d_status, (torch.int32,), "d_status", 1), _host_ptr(host_norm, (torch.float32,), "host_norm", 1),
+        _stream(stream))
+    _check(st, "mp_optimizer_step")
+
+
 def mp_outlier_state_bytes() -> int:
     return int(_lib.mp_outlier_state_bytes())
 
@@ -266,6 +312,7 @@ class Optimizer:
         self.n = self.table.total
         self.hyper = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
         self.clip = clip
+        self.hyper_struct = MpHyper(lr, beta1, beta2, eps, weight_decay, clip)
         dev = torch.device("cuda") if device is None else torch.device(device)
         nbytes = mp_grad_norm_workspace_bytes(self.n)
         self.workspace = torch.empty(max(8, nbytes), dtype=torch.uint8, device=dev)
@@ -274,12 +321,16 @@ class Optimizer:
         self.d_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.outlier = OutlierDetector(outlier_z, device=dev) if outlier_z is not None else None
 
-    def step(self, params, grads, master, m, v, t: int, seed: int, stream=None):
-        mp_grad_norm(grads, self.clip, self.workspace, self.d_norm, self.d_scale, n=self.n, stream=stream)
-        if self.outlier is not None:
-            self.outlier.check(self.d_norm, self.d_scale, self.d_status, stream=stream)
-        mp_adamw_step(params, grads, master, m, v, self.table, d_grad_scale=self.d_scale, t=t, seed=seed,
-                      d_status=self.d_status, n=self.n, stream=stream, **self.hyper)
+    def step(self, params, grads, master, m, v, t: int, seed: int, host_grads=None, host_norm=None, stream=None):
+        """One native call (mp_optimizer_step). With host_grads (pinned CPU
+        bf16), `grads` is the device buffer that receives them."""
+        mp_optimizer_step(params, grads, master, m, v, self.table, self.hyper_struct, t=t, seed=seed,
+                          workspace=self.workspace, d_norm=self.d_norm, d_scale=self.d_scale,
+                          d_status=self.d_status,
+                          outlier_state=self.outlier.state if self.outlier is not None else None,
+                          outlier_z=self.outlier.z_threshold if self.outlier is not None else 0.0,
+                          d_z=self.outlier.d_z if self.outlier is not None else None,
+                          host_grads=host_grads, host_norm=host_norm, n=self.n, stream=stream)
 
     def take_status(self) -> int:
         """Device status of the steps since the last call (0, MP_ERR_NONFINITE
@@ -296,7 +347,7 @@ class Optimizer:
 
 
 __all__ = [
-    "MpError", "MpTensor", "TensorTable", "Optimizer", "OutlierDetector", "mp_outlier_state_bytes",
+    "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "mp_optimizer_step", "OutlierDetector", "mp_outlier_state_bytes",
     "mp_outlier_reset", "mp_outlier_check", "lib", "abi_version", "status_string",
     "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc", "mp_adamw_step",
     "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",

@@ -60,6 +60,7 @@ const char* mp_status_string(int status) {
     case MP_ERR_CUDA: return "MP_ERR_CUDA: a CUDA runtime call failed";
     case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE: workspace missing or too small";
     case MP_SKIPPED_OUTLIER: return "MP_SKIPPED_OUTLIER: the grad-norm z-score was above the threshold; step skipped";
+    case MP_ERR_ACCESS: return "MP_ERR_ACCESS: host buffer is not page-locked memory the device can read";
     default: return "unknown mp_status";
   }
 }
@@ -93,11 +94,25 @@ int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip, void* workspace,
   return MP_OK;
 }
 
-int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
-                  uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
-                  float lr, float beta1, float beta2, float eps, float weight_decay, const float* d_grad_scale,
-                  int32_t t, uint32_t seed, int32_t* d_status, void* stream) {
-  if (n == 0) return MP_OK;
+}  // extern "C"
+
+namespace {
+
+// A validated step: decay segments over [lo, hi) and the launch scalars.
+struct StepPlan {
+  std::vector<uint64_t> seg_end;
+  std::vector<int> seg_flag;
+  mpk::StepArgs base{};
+  uint64_t lo = 0, hi = 0;
+  bool vec = false;
+};
+
+// Argument checks, host scalars and decay segments of one AdamW step. Makes
+// no CUDA call, so a failure leaves the stream untouched.
+int plan_step(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v, uint64_t global_offset,
+              uint64_t n, const mp_tensor_t* table, int32_t n_tensors, float lr, float beta1, float beta2, float eps,
+              float weight_decay, const float* d_grad_scale, int32_t t, uint32_t seed, int32_t* d_status,
+              StepPlan* plan) {
   if (params == nullptr || grads == nullptr || m == nullptr || v == nullptr || table == nullptr)
     return MP_ERR_NULL;
   if (!aligned(params, 2) || !aligned(grads, 2) || !aligned(master, 4) || !aligned(m, 4) || !aligned(v, 4) ||
@@ -118,25 +133,26 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float*
     off += T.size;
     if (off > kMaxN) return MP_ERR_TABLE;
   }
-  const uint64_t lo = global_offset, hi = global_offset + n;
-  if (off < hi) return MP_ERR_TABLE;
+  plan->lo = global_offset;
+  plan->hi = global_offset + n;
+  if (off < plan->hi) return MP_ERR_TABLE;
 
   // Decay segments over [lo, hi): maximal runs of equal flag, so flags alternate.
-  std::vector<uint64_t> seg_end;
-  std::vector<int> seg_flag;
+  plan->seg_end.clear();
+  plan->seg_flag.clear();
   for (int32_t k = 0; k < n_tensors; ++k) {
     const uint64_t a = table[k].offset, b = table[k].offset + table[k].size;
-    if (b <= lo || a >= hi || a == b) continue;
-    const uint64_t end = b < hi ? b : hi;
-    if (!seg_flag.empty() && seg_flag.back() == table[k].decay) {
-      seg_end.back() = end;
+    if (b <= plan->lo || a >= plan->hi || a == b) continue;
+    const uint64_t end = b < plan->hi ? b : plan->hi;
+    if (!plan->seg_flag.empty() && plan->seg_flag.back() == table[k].decay) {
+      plan->seg_end.back() = end;
     } else {
-      seg_end.push_back(end);
-      seg_flag.push_back(table[k].decay);
+      plan->seg_end.push_back(end);
+      plan->seg_flag.push_back(table[k].decay);
     }
   }
 
-  mpk::StepArgs base{};
+  mpk::StepArgs& base = plan->base;
   base.d_scale = d_grad_scale;
   base.d_status = d_status;
   base.lr = lr;
@@ -147,16 +163,16 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float*
   base.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(t)));
   base.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(t)));
   base.seed = seed;
+  plan->vec = aligned(params, 8) && aligned(grads, 8) && aligned(master, 16) && aligned(m, 16) && aligned(v, 16);
+  return MP_OK;
+}
 
-  mpk::DeviceInfo dev;
-  cudaError_t e = mpk::device_info(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  const bool vec = aligned(params, 8) && aligned(grads, 8) && aligned(master, 16) && aligned(m, 16) &&
-                   aligned(v, 16);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  // One launch per chunk of at most kSegCapLarge segments; chunk starts stay
-  // multiples of 4 elements from `lo` so vector alignment is preserved.
+// One launch per chunk of at most kSegCapLarge segments; chunk starts stay
+// multiples of 4 elements from `lo` so vector alignment is preserved.
+cudaError_t launch_step(const StepPlan& plan, uint16_t* params, const uint16_t* grads, float* master, float* m,
+                        float* v, const mpk::DeviceInfo& dev, cudaStream_t s) {
+  const std::vector<uint64_t>& seg_end = plan.seg_end;
+  const uint64_t lo = plan.lo, hi = plan.hi;
   const size_t ns = seg_end.size();
   uint64_t c0 = lo;
   size_t s0 = 0;
@@ -172,7 +188,7 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float*
       last = s0;
       while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
     }
-    mpk::StepArgs a = base;
+    mpk::StepArgs a = plan.base;
     const uint64_t d = c0 - lo;
     a.params = params + d;
     a.grads = grads + d;
@@ -182,14 +198,84 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float*
     a.n = c1 - c0;
     a.goff = c0;
     a.nseg = static_cast<uint32_t>(last - s0 + 1);
-    a.first_decay = static_cast<uint32_t>(seg_flag[s0]);
+    a.first_decay = static_cast<uint32_t>(plan.seg_flag[s0]);
     std::vector<uint64_t> ends(seg_end.begin() + s0, seg_end.begin() + last + 1);
     ends.back() = c1;
-    e = mpk::launch_adamw(a, ends.data(), vec, dev, s);
-    if (e != cudaSuccess) return cuda_fail(e);
+    const cudaError_t e = mpk::launch_adamw(a, ends.data(), plan.vec, dev, s);
+    if (e != cudaSuccess) return e;
     c0 = c1;
     while (s0 < ns && seg_end[s0] <= c0) ++s0;
   }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
+                  uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                  float lr, float beta1, float beta2, float eps, float weight_decay, const float* d_grad_scale,
+                  int32_t t, uint32_t seed, int32_t* d_status, void* stream) {
+  if (n == 0) return MP_OK;
+  StepPlan plan;
+  const int st = plan_step(params, grads, master, m, v, global_offset, n, table, n_tensors, lr, beta1, beta2, eps,
+                           weight_decay, d_grad_scale, t, seed, d_status, &plan);
+  if (st != MP_OK) return st;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_step(plan, params, grads, master, m, v, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads, float* master, float* m,
+                      float* v, uint64_t n, const mp_tensor_t* table, int32_t n_tensors, const mp_hyper_t* hyper,
+                      int32_t t, uint32_t seed, void* workspace, size_t workspace_bytes, void* outlier_state,
+                      float outlier_z, double* d_z, float* d_norm, float* d_scale, int32_t* d_status,
+                      float* host_norm, void* stream) {
+  if (hyper == nullptr || d_norm == nullptr || d_scale == nullptr) return MP_ERR_NULL;
+  if (workspace == nullptr) return MP_ERR_WORKSPACE;
+  if (!aligned(workspace, 8) || !aligned(d_norm, 4) || !aligned(d_scale, 4) || !aligned(outlier_state, 8) ||
+      !aligned(d_z, 8) || !aligned(host_grads, 2) || !aligned(host_norm, 4))
+    return MP_ERR_ALIGN;
+  if (!(hyper->clip > 0.0f) || !std::isfinite(hyper->clip)) return MP_ERR_RANGE;
+  StepPlan plan;
+  if (n != 0) {
+    const int st = plan_step(params, grads, master, m, v, 0, n, table, n_tensors, hyper->lr, hyper->beta1,
+                             hyper->beta2, hyper->eps, hyper->weight_decay, d_scale, t, seed, d_status, &plan);
+    if (st != MP_OK) return st;
+  }
+  // Host gradients must be page-locked: their device-visible address is read
+  // by the norm kernel, which also writes the device copy into `grads`.
+  const uint16_t* src = grads;
+  if (host_grads != nullptr && n != 0) {
+    cudaPointerAttributes attr{};
+    const cudaError_t e = cudaPointerGetAttributes(&attr, host_grads);
+    if (e != cudaSuccess) {
+      cudaGetLastError();  // clear the non-sticky error this query may leave
+      return MP_ERR_ACCESS;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return MP_ERR_ACCESS;
+    src = static_cast<const uint16_t*>(attr.devicePointer);
+  }
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool copy = host_grads != nullptr && n != 0;
+  const bool vec = aligned(src, 16) && (!copy || aligned(grads, 16));
+  const int nb = mpk::norm_blocks(n, vec, dev);
+  if (workspace_bytes < sizeof(double) * static_cast<size_t>(nb)) return MP_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = mpk::launch_norm(src, n, vec, static_cast<double*>(workspace), nb, hyper->clip, d_norm, d_scale, nullptr,
+                       s, copy ? grads : nullptr);
+  if (e == cudaSuccess && outlier_state != nullptr)
+    e = mpk::launch_outlier_check(outlier_state, d_norm, outlier_z, d_scale, d_z, d_status, s);
+  if (e == cudaSuccess && n != 0) e = launch_step(plan, params, grads, master, m, v, dev, s);
+  if (e == cudaSuccess && host_norm != nullptr)
+    e = cudaMemcpyAsync(host_norm, d_norm, sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   return MP_OK;
 }
 

@@ -65,9 +65,15 @@ cudaError_t launch_adamw(const StepArgs& a, const uint64_t* seg_end, bool vec,
                          const DeviceInfo& dev, cudaStream_t stream);
 
 int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev);
+// copy_out != nullptr: grads may be page-locked host memory (device-visible
+// address); the kernel also writes every gradient to copy_out (device).
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials,
                         int nblocks, float clip, float* d_norm, float* d_scale,
-                        double* d_sumsq, cudaStream_t stream);
+                        double* d_sumsq, cudaStream_t stream, uint16_t* copy_out = nullptr);
+
+// Outlier check of the grad norm (mp_outlier.cu): d_state holds the window.
+cudaError_t launch_outlier_check(void* d_state, const float* d_norm, float z_threshold, float* d_scale,
+                                 double* d_z, int32_t* d_status, cudaStream_t stream);
 
 cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
                       uint32_t seed, bool vec, const DeviceInfo& dev, cudaStream_t stream);

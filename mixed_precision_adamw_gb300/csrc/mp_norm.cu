@@ -78,12 +78,19 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
   return r;
 }
 
-// vec: grads 16-B aligned, processed as 8-element vectors plus a scalar tail.
+// vec: grads (and copy_out) 16-B aligned, processed as 8-element vectors
+// plus a scalar tail. kCopy: grads may live in page-locked host memory (read
+// over the host link) and every element read is also written to copy_out, so
+// the host-to-device transfer and the norm are one pass; the arithmetic and
+// its order are the same as without the copy.
+template <bool kCopy>
 __global__ void __launch_bounds__(kThreads)
-norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, double* __restrict__ partials) {
+norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, double* __restrict__ partials,
+                    uint16_t* __restrict__ copy_out) {
   __shared__ double sh[kThreads / 32 + 1];
   pdl_enter();
   const uint4* g4 = reinterpret_cast<const uint4*>(grads);
+  uint4* c4 = reinterpret_cast<uint4*>(copy_out);
   const uint64_t nvec = vec ? n / 8 : 0;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   const uint64_t k0 = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -94,21 +101,35 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
     uint4 w[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) w[u] = __ldcs(g4 + k + u * stride);
+    if (kCopy) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) c4[k + u * stride] = w[u];
+    }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) acc(s, c, sumsq8(w[u]));
   }
-  for (; k < nvec; k += stride) acc(s, c, sumsq8(__ldcs(g4 + k)));
+  for (; k < nvec; k += stride) {
+    const uint4 w = __ldcs(g4 + k);
+    if (kCopy) c4[k] = w;
+    acc(s, c, sumsq8(w));
+  }
   for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
-    const float x = bf16_to_f32(grads[i]);
+    const uint16_t h = grads[i];
+    if (kCopy) copy_out[i] = h;
+    const float x = bf16_to_f32(h);
     acc(s, c, __fmul_rn(x, x));
   }
   double S = block_sum(__dadd_rn(static_cast<double>(s), static_cast<double>(c)), sh);
 
   if (!(S <= DBL_MAX) || S < 0x1p-60) {  // uniform across the block: S is a broadcast value
+    // Re-read this thread's own elements (from the device copy when there is
+    // one: a thread always sees its own earlier writes).
+    const uint4* r4 = kCopy ? reinterpret_cast<const uint4*>(copy_out) : g4;
+    const uint16_t* r1 = kCopy ? copy_out : grads;
     double d = 0.0;
-    for (k = k0; k < nvec; k += stride) d = __dadd_rn(d, dsumsq8(__ldcs(g4 + k)));
+    for (k = k0; k < nvec; k += stride) d = __dadd_rn(d, dsumsq8(r4[k]));
     for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
-      const double x = bf16_to_f32(grads[i]);
+      const double x = bf16_to_f32(r1[i]);
       d = __dadd_rn(d, __dmul_rn(x, x));
     }
     S = block_sum(d, sh);
@@ -151,9 +172,13 @@ int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev) {
 }
 
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials, int nblocks,
-                        float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream) {
-  cudaError_t e = launch_pdl(norm_partial_kernel, static_cast<unsigned>(nblocks), kThreads, stream, grads, n,
-                             vec ? 1 : 0, partials);
+                        float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream,
+                        uint16_t* copy_out) {
+  cudaError_t e = copy_out == nullptr
+                      ? launch_pdl(norm_partial_kernel<false>, static_cast<unsigned>(nblocks), kThreads, stream,
+                                   grads, n, vec ? 1 : 0, partials, copy_out)
+                      : launch_pdl(norm_partial_kernel<true>, static_cast<unsigned>(nblocks), kThreads, stream,
+                                   grads, n, vec ? 1 : 0, partials, copy_out);
   if (e != cudaSuccess) return e;
   return launch_pdl(norm_finalize_kernel, 1u, kThreads, stream, static_cast<const double*>(partials), nblocks,
                     clip, d_norm, d_scale, d_sumsq);

@@ -60,6 +60,13 @@ __global__ void outlier_check_kernel(OutlierState* st, const float* d_norm, floa
 }
 
 }  // namespace
+
+cudaError_t launch_outlier_check(void* d_state, const float* d_norm, float z_threshold, float* d_scale,
+                                 double* d_z, int32_t* d_status, cudaStream_t stream) {
+  return launch_pdl(outlier_check_kernel, 1u, 1u, stream, static_cast<OutlierState*>(d_state), d_norm,
+                    z_threshold, d_scale, d_z, d_status);
+}
+
 }  // namespace mpk
 
 extern "C" size_t mp_outlier_state_bytes(void) { return sizeof(mpk::OutlierState); }
@@ -80,9 +87,8 @@ extern "C" int mp_outlier_check(void* d_state, const float* d_norm, float z_thre
       reinterpret_cast<uintptr_t>(d_scale) % 4 || reinterpret_cast<uintptr_t>(d_z) % 8 ||
       reinterpret_cast<uintptr_t>(d_status) % 4)
     return MP_ERR_ALIGN;
-  const cudaError_t e = mpk::launch_pdl(mpk::outlier_check_kernel, 1u, 1u, static_cast<cudaStream_t>(stream),
-                                        static_cast<mpk::OutlierState*>(d_state), d_norm, z_threshold, d_scale,
-                                        d_z, d_status);
+  const cudaError_t e = mpk::launch_outlier_check(d_state, d_norm, z_threshold, d_scale, d_z, d_status,
+                                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return mpk::record_cuda_error(e);
   return MP_OK;
 }

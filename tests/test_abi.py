@@ -117,3 +117,33 @@ def test_product_never_touches_the_oracle():
         if fn.endswith((".c", ".h", ".py")):
             text = open(os.path.join(ROOT, "oracle", fn)).read()
             assert "mixed_precision_adamw_gb300" not in text and "mp_adamw.h" not in text
+
+
+def test_optimizer_step_argument_checks(mp):
+    L = mp.lib()
+    tab = mp.TensorTable([(0, 100, 1)])
+    hyper = mp.MpHyper(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    bad_clip = mp.MpHyper(1e-3, 0.9, 0.95, 1e-8, 0.1, 0.0)
+    bad_beta = mp.MpHyper(1e-3, 1.0, 0.95, 1e-8, 0.1, 1.0)
+
+    def call(**kw):
+        a = dict(params=FAKE, grads=FAKE, host=None, master=FAKE, m=FAKE, v=FAKE, n=100, hyper=hyper, t=1,
+                 ws=FAKE, wsb=4096, ost=None, z=0.0, dz=None, norm=FAKE, scale=FAKE, status=None, hnorm=None)
+        a.update(kw)
+        return L.mp_optimizer_step(a["params"], a["grads"], a["host"], a["master"], a["m"], a["v"], a["n"],
+                                   tab.ctypes_array, tab.n_tensors,
+                                   ctypes.byref(a["hyper"]) if a["hyper"] is not None else None, a["t"], 3,
+                                   a["ws"], a["wsb"], a["ost"], a["z"], a["dz"], a["norm"], a["scale"],
+                                   a["status"], a["hnorm"], None)
+    assert call(hyper=None) == mp.MP_ERR_NULL
+    assert call(norm=None) == mp.MP_ERR_NULL
+    assert call(ws=None) == mp.MP_ERR_WORKSPACE
+    assert call(hyper=bad_clip) == mp.MP_ERR_RANGE
+    assert call(hyper=bad_beta) == mp.MP_ERR_RANGE
+    assert call(t=0) == mp.MP_ERR_RANGE
+    assert call(params=None) == mp.MP_ERR_NULL
+    assert call(ost=FAKE + 4) == mp.MP_ERR_ALIGN
+    assert call(dz=FAKE + 4) == mp.MP_ERR_ALIGN
+    assert call(host=FAKE + 1) == mp.MP_ERR_ALIGN
+    assert call(n=101) == mp.MP_ERR_TABLE
+    assert mp.status_string(mp.MP_ERR_ACCESS).startswith("MP_ERR_ACCESS")
