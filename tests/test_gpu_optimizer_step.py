@@ -90,3 +90,58 @@ def test_pageable_host_gradients_are_refused():
     torch.cuda.synchronize()
     for k in st:
         assert _same(st[k], before[k]), k
+
+
+@pytest.mark.parametrize("host_off,dev_off,n", [(1, 1, 2048 * 5 + 7), (1, 0, 100003), (0, 3, 4099), (0, 0, 7)])
+def test_host_gradients_unaligned_and_ragged(host_off, dev_off, n):
+    """Unaligned host or device buffers take the element-wise copy path; the
+    result must equal the same step on device gradients bit for bit, and the
+    landing buffer must not be written outside its n elements."""
+    gen = torch.Generator().manual_seed(n + host_off)
+    tab = W.random_table(n, gen, 1, 3000)
+    g_cpu = (torch.randn(n, generator=gen) * 1e-2).to(torch.bfloat16)
+    master = (torch.randn(n, generator=gen) * 0.05).cuda()
+    st = dict(params=master.to(torch.bfloat16), master=master, m=torch.zeros_like(master), v=torch.zeros_like(master))
+    host = torch.empty(n + host_off, dtype=torch.bfloat16, pin_memory=True)
+    host[host_off:].copy_(g_cpu)
+    guard = 4096
+    land_buf = torch.full((n + dev_off + 2 * guard,), 0x5A5A, dtype=torch.int16, device="cuda")
+    landing = land_buf[guard + dev_off:guard + dev_off + n].view(torch.bfloat16)
+    H = W.HYPER
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
+    a = {k: x.clone() for k, x in st.items()}
+    b = {k: x.clone() for k, x in st.items()}
+    opt_a = mp.Optimizer(tab, clip=H["clip"], **kw)
+    opt_b = mp.Optimizer(tab, clip=H["clip"], **kw)
+    opt_a.step(a["params"], g_cpu.cuda(), a["master"], a["m"], a["v"], 3, 5)
+    opt_b.step(b["params"], landing, b["master"], b["m"], b["v"], 3, 5, host_grads=host[host_off:])
+    torch.cuda.synchronize()
+    assert _same(landing, g_cpu.cuda())
+    h = land_buf.cpu()
+    assert torch.all(h[:guard + dev_off] == 0x5A5A) and torch.all(h[guard + dev_off + n:] == 0x5A5A)
+    assert opt_a.d_norm.item() == opt_b.d_norm.item()
+    for k in a:
+        assert _same(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e25])
+def test_host_gradients_extreme_values_take_the_fp64_path(scale):
+    """Blocks whose fp32 squares underflow or overflow recompute in fp64 from
+    the device copy; the norm must match the device-gradient path."""
+    n = 3 * 2048 * 152 + 11
+    g_cpu = (torch.randn(n, generator=torch.Generator().manual_seed(1)) * scale).to(torch.bfloat16)
+    host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    host.copy_(g_cpu)
+    master = torch.zeros(n, device="cuda")
+    st = dict(params=master.to(torch.bfloat16), master=master, m=torch.zeros_like(master), v=torch.zeros_like(master))
+    opt_a = mp.Optimizer([(0, n, 1)], lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip=1.0)
+    opt_b = mp.Optimizer([(0, n, 1)], lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip=1.0)
+    landing = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    a = {k: x.clone() for k, x in st.items()}
+    b = {k: x.clone() for k, x in st.items()}
+    opt_a.step(a["params"], g_cpu.cuda(), a["master"], a["m"], a["v"], 1, 2)
+    opt_b.step(b["params"], landing, b["master"], b["m"], b["v"], 1, 2, host_grads=host)
+    torch.cuda.synchronize()
+    assert opt_a.d_norm.item() == opt_b.d_norm.item() and np.isfinite(opt_a.d_norm.item())
+    for k in a:
+        assert _same(a[k], b[k]), k

@@ -303,6 +303,23 @@ def test_step_global_offset_across_2_pow_32(goff):
     _compare(d, host, f"offset {goff}")
 
 
+@pytest.mark.parametrize("nseg", [31, 32, 33, 1023, 1024, 1025])
+def test_step_segment_table_size_boundaries(nseg):
+    """Tables right at and past the two kernel-parameter table sizes (32 and
+    1024 decay segments); 1025 segments split into two launches."""
+    seg = 53
+    n = nseg * seg
+    tab = [(k * seg, seg, k % 2) for k in range(nseg)]
+    _, params, grads, master, m, v = _random_case(n, nseg)
+    d = dict(params=dev_u16(params), grads=dev_u16(grads), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master))
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=1e-2,
+                     beta1=0.9, beta2=0.99, eps=1e-8, weight_decay=0.5, d_grad_scale=None, t=4, seed=nseg)
+    host = dict(params=params.copy(), master=master.copy(), m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, 1e-2, 0.9, 0.99,
+                             1e-8, 0.5, 1.0, 4, nseg) == 0
+    _compare(d, host, f"{nseg} segments")
+
+
 def test_step_many_segments_split_into_launches():
     """A table with 5000 alternating-decay tensors (more segments than one
     launch carries) gives the same result as the oracle."""
