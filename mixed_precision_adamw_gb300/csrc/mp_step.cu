@@ -119,9 +119,10 @@ __device__ __forceinline__ bool read_scale(const StepArgs& p, float& scale) {
 }
 
 // Resident blocks per SM the vector kernel is compiled for: the with-master
-// kernel keeps 3 blocks of 256 threads (its 68 registers; forcing 4 was 8 %
-// slower on GB300), the no-master kernel moves fewer bytes per element and
-// runs 9 % faster at 4 blocks (64 registers), where more warps hide latency.
+// kernel keeps 3 blocks of 256 threads (it compiles to 76 registers; forcing 4
+// blocks, i.e. at most 64 registers, was 8 % slower on GB300); the no-master
+// kernel moves fewer bytes per element and runs 9 % faster at 4 blocks (63
+// registers), where the extra warps hide more memory latency.
 template <bool kMaster>
 struct VecOccupancy {
   static constexpr int kMinBlocks = kMaster ? 3 : 4;
