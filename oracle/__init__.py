@@ -32,43 +32,47 @@ class OracleOutlier(ctypes.Structure):
 _lib = None
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Load an oracle build from `path` with its function signatures set."""
+    L = ctypes.CDLL(path)
+    L.oracle_noise_u32.restype = ctypes.c_uint32
+    L.oracle_noise_u32.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_noise_fill.restype = None
+    L.oracle_noise_fill.argtypes = [_c_u32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_sr_with_rand.restype = ctypes.c_uint16
+    L.oracle_sr_with_rand.argtypes = [ctypes.c_float, ctypes.c_uint32]
+    L.oracle_sr.restype = ctypes.c_uint16
+    L.oracle_sr.argtypes = [ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_stochastic_round.restype = None
+    L.oracle_stochastic_round.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64,
+                                          ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_sumsq.restype = ctypes.c_double
+    L.oracle_sumsq.argtypes = [_c_u16p, ctypes.c_uint64]
+    L.oracle_clip_scale.restype = ctypes.c_float
+    L.oracle_clip_scale.argtypes = [ctypes.c_float, ctypes.c_float]
+    L.oracle_grad_norm.restype = None
+    L.oracle_grad_norm.argtypes = [_c_u16p, ctypes.c_uint64, ctypes.c_float,
+                                   _c_f64p, _c_f32p, _c_f32p]
+    L.oracle_bias_corrections.restype = None
+    L.oracle_bias_corrections.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int32,
+                                          _c_f32p, _c_f32p]
+    L.oracle_adamw_step.restype = ctypes.c_int
+    L.oracle_adamw_step.argtypes = [
+        _c_u16p, _c_u16p, _c_f32p, _c_f32p, _c_f32p,
+        ctypes.c_uint64, ctypes.c_uint64,
+        ctypes.POINTER(OracleTensor), ctypes.c_int32,
+        ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+        ctypes.c_float, ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
+    L.oracle_outlier_check.restype = ctypes.c_int
+    L.oracle_outlier_check.argtypes = [ctypes.POINTER(OracleOutlier), ctypes.c_float, ctypes.c_float,
+                                       _c_f32p, _c_f64p]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
-        L = ctypes.CDLL(path)
-        L.oracle_noise_u32.restype = ctypes.c_uint32
-        L.oracle_noise_u32.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
-        L.oracle_noise_fill.restype = None
-        L.oracle_noise_fill.argtypes = [_c_u32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
-        L.oracle_sr_with_rand.restype = ctypes.c_uint16
-        L.oracle_sr_with_rand.argtypes = [ctypes.c_float, ctypes.c_uint32]
-        L.oracle_sr.restype = ctypes.c_uint16
-        L.oracle_sr.argtypes = [ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32]
-        L.oracle_stochastic_round.restype = None
-        L.oracle_stochastic_round.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64,
-                                              ctypes.c_uint64, ctypes.c_uint32]
-        L.oracle_sumsq.restype = ctypes.c_double
-        L.oracle_sumsq.argtypes = [_c_u16p, ctypes.c_uint64]
-        L.oracle_clip_scale.restype = ctypes.c_float
-        L.oracle_clip_scale.argtypes = [ctypes.c_float, ctypes.c_float]
-        L.oracle_grad_norm.restype = None
-        L.oracle_grad_norm.argtypes = [_c_u16p, ctypes.c_uint64, ctypes.c_float,
-                                       _c_f64p, _c_f32p, _c_f32p]
-        L.oracle_bias_corrections.restype = None
-        L.oracle_bias_corrections.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int32,
-                                              _c_f32p, _c_f32p]
-        L.oracle_adamw_step.restype = ctypes.c_int
-        L.oracle_adamw_step.argtypes = [
-            _c_u16p, _c_u16p, _c_f32p, _c_f32p, _c_f32p,
-            ctypes.c_uint64, ctypes.c_uint64,
-            ctypes.POINTER(OracleTensor), ctypes.c_int32,
-            ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
-            ctypes.c_float, ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
-        L.oracle_outlier_check.restype = ctypes.c_int
-        L.oracle_outlier_check.argtypes = [ctypes.POINTER(OracleOutlier), ctypes.c_float, ctypes.c_float,
-                                           _c_f32p, _c_f64p]
-        _lib = L
+        _lib = load_library(_build.build())
     return _lib
 
 

@@ -263,8 +263,13 @@ def test_sr_special_values():
     assert oracle.sr_with_rand(0.0, 0) == 0x0000
     assert oracle.sr_with_rand(-0.0, 0) == 0x8000
     assert oracle.sr_with_rand(float("nan"), 0xFFFF) == 0x7FC0
-    nan_low = np.array([0x7F800001], np.uint32).view(np.float32)[0]
-    assert oracle.sr_with_rand(float(nan_low), 0xFFFF) == 0x7FC0
+    # NaNs whose payload lies only in the low 16 bits would truncate to an
+    # infinity; pass their raw patterns through the array entry point (a
+    # Python float would quiet them and set a high payload bit)
+    nans = np.array([0x7F800001, 0xFF800003, 0x7F80FFFF, 0xFF80FFFF, 0x7FC00000, 0x7FFFFFFF],
+                    np.uint32).view(np.float32)
+    for seed in range(4):
+        assert np.all(oracle.stochastic_round(nans, 1000 * seed, seed) == 0x7FC0)
     # the largest finite fp32 rounds to bf16 max or to +Inf (carry into the exponent)
     big = float(np.finfo(np.float32).max)
     assert oracle.sr_with_rand(big, 0xFFFF) == 0x7F7F
