@@ -297,12 +297,14 @@ class OutlierDetector:
 
 
 class Optimizer:
-    """Convenience wrapper holding the device state of one optimizer step:
-    workspace, norm/scale/status scalars and the packed tensor table.
+    """The device state of the optimizer step: workspace, norm/scale/status
+    scalars, the packed tensor table and (with outlier_z) the outlier window.
 
-    step() enqueues mp_grad_norm then mp_adamw_step on the current stream and
-    does not synchronise; call check_status() after a sync to learn whether a
-    step was refused for a non-finite norm.
+    step() makes one mp_optimizer_step call on the given (default: current)
+    stream — norm and clip scale, the optional outlier check, the AdamW + SR
+    update — and does not synchronise. take_status() (which synchronises)
+    tells whether a step was refused for a non-finite norm or skipped as an
+    outlier; check_status() raises MpError instead.
     """
 
     def __init__(self, table_entries: Sequence[Tuple[int, int, int]], *, lr: float, beta1: float,
@@ -347,8 +349,8 @@ class Optimizer:
 
 
 __all__ = [
-    "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "mp_optimizer_step", "OutlierDetector", "mp_outlier_state_bytes",
-    "mp_outlier_reset", "mp_outlier_check", "lib", "abi_version", "status_string",
-    "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc", "mp_adamw_step",
+    "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "OutlierDetector", "lib", "abi_version",
+    "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
+    "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
     "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",
 ]
