@@ -108,10 +108,16 @@ def measured_hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the step kernel's code with comments and blank space removed,
+    so that editing a comment does not invalidate recorded counters."""
     h = hashlib.sha256()
     for rel in STEP_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.strip() for line in text.splitlines() if line.strip())
+        h.update(text.encode())
     return h.hexdigest()[:16]
 
 
