@@ -1,0 +1,146 @@
+/*
+ * c_abi_check.c — drives libmpadamw.so from plain C (no Python, no PyTorch)
+ * and checks the results against the CPU oracle compiled into the same
+ * program. Test code: it allocates its own device buffers with cudaMalloc.
+ *
+ * One optimizer step (mp_optimizer_step, then a second call of the pieces:
+ * mp_grad_norm + mp_adamw_step) on n = 100,003 elements split into 7 tensors
+ * with alternating decay flags, then mp_stochastic_round. Exit status 0 when
+ * every output is bit-identical to the oracle's.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "mp_adamw.h"
+#include "mp_oracle.h"
+
+#define N 100003u
+#define NT 7
+
+static uint64_t rng_state = 0x9E3779B97F4A7C15ull;
+static uint32_t rng_u32(void) { /* xorshift64*: seeded synthetic inputs */
+    rng_state ^= rng_state >> 12;
+    rng_state ^= rng_state << 25;
+    rng_state ^= rng_state >> 27;
+    return (uint32_t)((rng_state * 0x2545F4914F6CDD1Dull) >> 32);
+}
+static float rng_uniform(void) { return (float)(rng_u32() >> 8) / 16777216.0f - 0.5f; }
+static uint16_t to_bf16_bits(float x) { /* truncation: any bf16 pattern is a valid input */
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    return (uint16_t)(u >> 16);
+}
+
+#define CK(call) do { cudaError_t e_ = (call); if (e_ != cudaSuccess) { \
+    fprintf(stderr, "%s: %s\n", #call, cudaGetErrorString(e_)); return 2; } } while (0)
+#define MP(call) do { int s_ = (call); if (s_ != MP_OK) { \
+    fprintf(stderr, "%s: %s\n", #call, mp_status_string(s_)); return 3; } } while (0)
+
+static int same(const void* a, const void* b, size_t bytes, const char* what) {
+    if (memcmp(a, b, bytes) != 0) {
+        fprintf(stderr, "%s differs from the oracle\n", what);
+        return 0;
+    }
+    return 1;
+}
+
+int main(void) {
+    static uint16_t params[N], grads[N], params_o[N], out_sr[N], out_sr_o[N];
+    static float master[N], m[N], v[N], master_o[N], m_o[N], v_o[N];
+    for (uint32_t i = 0; i < N; ++i) {
+        master[i] = 0.05f * rng_uniform();
+        params[i] = to_bf16_bits(master[i]);
+        grads[i] = to_bf16_bits(0.02f * rng_uniform());
+        m[i] = 1e-3f * rng_uniform();
+        v[i] = 1e-6f * (rng_uniform() + 0.5f);
+    }
+    mp_tensor_t table[NT];
+    oracle_tensor otable[NT];
+    uint64_t off = 0;
+    for (int k = 0; k < NT; ++k) {
+        uint64_t size = (k == NT - 1) ? N - off : (uint64_t)(N / NT + 17 * k);
+        table[k].offset = off; table[k].size = size; table[k].decay = k % 2; table[k].reserved = 0;
+        otable[k].offset = off; otable[k].size = size; otable[k].decay = k % 2; otable[k].pad = 0;
+        off += size;
+    }
+    memcpy(params_o, params, sizeof params);
+    memcpy(master_o, master, sizeof master);
+    memcpy(m_o, m, sizeof m);
+    memcpy(v_o, v, sizeof v);
+
+    uint16_t *d_params, *d_grads, *d_sr;
+    float *d_master, *d_m, *d_v, *d_norm, *d_scale;
+    int32_t* d_status;
+    void* d_ws;
+    const size_t ws_bytes = mp_grad_norm_workspace_bytes(N);
+    CK(cudaMalloc((void**)&d_params, sizeof params));
+    CK(cudaMalloc((void**)&d_grads, sizeof grads));
+    CK(cudaMalloc((void**)&d_sr, sizeof out_sr));
+    CK(cudaMalloc((void**)&d_master, sizeof master));
+    CK(cudaMalloc((void**)&d_m, sizeof m));
+    CK(cudaMalloc((void**)&d_v, sizeof v));
+    CK(cudaMalloc((void**)&d_norm, 4));
+    CK(cudaMalloc((void**)&d_scale, 4));
+    CK(cudaMalloc((void**)&d_status, 4));
+    CK(cudaMalloc(&d_ws, ws_bytes));
+    CK(cudaMemcpy(d_params, params, sizeof params, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_grads, grads, sizeof grads, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_master, master, sizeof master, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_m, m, sizeof m, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(d_v, v, sizeof v, cudaMemcpyHostToDevice));
+    CK(cudaMemset(d_status, 0, 4));
+
+    const mp_hyper_t hyper = {1e-3f, 0.9f, 0.95f, 1e-8f, 0.1f, 1.0f};
+    /* step 1: the whole step in one call */
+    MP(mp_optimizer_step(d_params, d_grads, NULL, d_master, d_m, d_v, N, table, NT, &hyper, 1, 11,
+                         d_ws, ws_bytes, NULL, 0.0f, NULL, d_norm, d_scale, d_status, NULL, NULL));
+    float norm1, scale1;
+    CK(cudaMemcpy(&norm1, d_norm, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&scale1, d_scale, 4, cudaMemcpyDeviceToHost));
+    /* step 2: the same through the separate calls */
+    MP(mp_grad_norm(d_grads, N, hyper.clip, d_ws, ws_bytes, d_norm, d_scale, NULL, NULL));
+    MP(mp_adamw_step(d_params, d_grads, d_master, d_m, d_v, 0, N, table, NT, hyper.lr, hyper.beta1, hyper.beta2,
+                     hyper.eps, hyper.weight_decay, d_scale, 2, 12, d_status, NULL));
+    float scale2;
+    CK(cudaMemcpy(&scale2, d_scale, 4, cudaMemcpyDeviceToHost));
+    /* standalone rounding of the new master */
+    MP(mp_stochastic_round(d_sr, d_master, 0, N, 99, NULL));
+    int32_t status;
+    CK(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(params, d_params, sizeof params, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(master, d_master, sizeof master, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(m, d_m, sizeof m, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(v, d_v, sizeof v, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(out_sr, d_sr, sizeof out_sr, cudaMemcpyDeviceToHost));
+
+    /* the oracle, with the GPU's clip scales (the norms are checked to 1e-6) */
+    double sumsq;
+    float norm_o, scale_o;
+    oracle_grad_norm(grads, N, hyper.clip, &sumsq, &norm_o, &scale_o);
+    if (!(fabs((double)norm1 - sqrt(sumsq)) <= 1e-6 * sqrt(sumsq)) || scale1 != oracle_clip_scale(norm1, 1.0f)) {
+        fprintf(stderr, "norm %.9g vs oracle %.9g\n", norm1, sqrt(sumsq));
+        return 1;
+    }
+    if (oracle_adamw_step(params_o, grads, master_o, m_o, v_o, 0, N, otable, NT, hyper.lr, hyper.beta1,
+                          hyper.beta2, hyper.eps, hyper.weight_decay, scale1, 1, 11) != 0 ||
+        oracle_adamw_step(params_o, grads, master_o, m_o, v_o, 0, N, otable, NT, hyper.lr, hyper.beta1,
+                          hyper.beta2, hyper.eps, hyper.weight_decay, scale2, 2, 12) != 0)
+        return 1;
+    oracle_stochastic_round(out_sr_o, master_o, 0, N, 99);
+    int ok = status == 0;
+    ok &= same(params, params_o, sizeof params, "params");
+    ok &= same(master, master_o, sizeof master, "master");
+    ok &= same(m, m_o, sizeof m, "m");
+    ok &= same(v, v_o, sizeof v, "v");
+    ok &= same(out_sr, out_sr_o, sizeof out_sr, "stochastic round");
+    printf("c_abi_check: %s (n=%u, norm %.7g, scale %.7g)\n", ok ? "bit-identical to the oracle" : "MISMATCH",
+           N, norm1, scale1);
+    cudaFree(d_params); cudaFree(d_grads); cudaFree(d_sr); cudaFree(d_master); cudaFree(d_m); cudaFree(d_v);
+    cudaFree(d_norm); cudaFree(d_scale); cudaFree(d_status); cudaFree(d_ws);
+    return ok ? 0 : 1;
+}
