@@ -32,6 +32,9 @@
  *    fp32, 8 B for fp64) or the call returns MP_ERR_ALIGN. Buffers that are
  *    also 16-B aligned take the vectorised kernels; others take scalar
  *    kernels that compute bit-identical results more slowly.
+ *  - Input and output buffers of one call must not overlap (params, grads,
+ *    master, m and v are distinct arrays), and every device pointer must
+ *    belong to the current device (cudaSetDevice) of the calling thread.
  *  - Nothing in the library calls exit(), prints, or allocates device memory.
  */
 #ifndef MP_ADAMW_H

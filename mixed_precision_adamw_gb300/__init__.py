@@ -124,6 +124,8 @@ def _ptr(t: Optional[torch.Tensor], dtypes, name: str, n: Optional[int] = None) 
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_cuda:
         raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     if n is not None and t.numel() < n:
