@@ -61,3 +61,15 @@ def assert_bit_equal(gpu: np.ndarray, ref: np.ndarray, name: str):
 
 def rel_err(a: float, b: float) -> float:
     return abs(a - b) / abs(b) if b != 0 else abs(a - b)
+
+
+def assert_f32_bits_or_both_nan(gpu: np.ndarray, ref: np.ndarray, name: str):
+    """Bit equality, except that NaNs need only sit at the same positions:
+    arithmetic NaNs carry different payloads on the GPU and on host CPUs."""
+    gpu = np.asarray(gpu, np.float32)
+    ref = np.asarray(ref, np.float32)
+    gn, rn = np.isnan(gpu), np.isnan(ref)
+    assert np.array_equal(gn, rn), f"{name}: NaN positions differ ({int(gn.sum())} vs {int(rn.sum())})"
+    ok = ~gn
+    neq = bits32(gpu[ok]) != bits32(ref[ok])
+    assert not neq.any(), f"{name}: {int(neq.sum())} non-NaN elements differ bitwise"

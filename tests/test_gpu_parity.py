@@ -505,3 +505,42 @@ def test_resume_replay_is_bit_identical():
     for k in a:
         assert torch.equal(a[k].view(torch.int16) if k == "params" else a[k].view(torch.int32),
                            b[k].view(torch.int16) if k == "params" else b[k].view(torch.int32)), k
+
+
+@pytest.mark.parametrize("case", ["subnormal_moments", "overflowing_squares", "inf_nan_grads", "subnormal_weights"])
+def test_step_extreme_values(case):
+    """No flush-to-zero anywhere (subnormal moments and weights), squares that
+    overflow to Inf, and Inf/NaN gradients run through with a unit scale: the
+    bf16 weights match bit for bit (NaN is canonical there), fp32 state matches
+    bit for bit apart from NaN payloads."""
+    from helpers import assert_f32_bits_or_both_nan
+    rng = np.random.default_rng(31)
+    n = 2048 * 6 + 13
+    master = (rng.standard_normal(n) * 0.05).astype(np.float32)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    g = rng.standard_normal(n)
+    if case == "subnormal_moments":
+        g = g * 1e-22                     # g^2 ~ 1e-44: subnormal second moment
+    elif case == "overflowing_squares":
+        g = g * 1e20                      # g^2 overflows fp32
+    elif case == "inf_nan_grads":
+        g = g * 1e-2
+        g[::97] = np.inf
+        g[5::101] = -np.inf
+        g[7::89] = np.nan
+    else:
+        master = (rng.standard_normal(n) * 1e-39).astype(np.float32)  # subnormal weights, decayed
+        g = g * 1e-3
+    grads = bf16_from_f32(g)
+    params = bf16_from_f32(master)
+    tab = [(0, n // 2, 1), (n // 2, n - n // 2, 0)]
+    d = dict(params=dev_u16(params), grads=dev_u16(grads), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master))
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=1e-2,
+                     beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, d_grad_scale=None, t=1, seed=3)
+    host = dict(params=params.copy(), master=master.copy(), m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, 1e-2, 0.9, 0.95,
+                             1e-8, 0.1, 1.0, 1, 3) == 0
+    assert_bit_equal(to_np_u16(d["params"]), host["params"], f"{case} params")
+    for k in ("master", "m", "v"):
+        assert_f32_bits_or_both_nan(to_np_f32(d[k]), host[k], f"{case} {k}")
