@@ -54,6 +54,7 @@ STEP_BYTES_NOMASTER = 22
 NORM_BYTES = 2
 SR_BYTES = 6
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only)
 STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
                        "mixed_precision_adamw_gb300/csrc/mp_device.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
@@ -259,9 +260,13 @@ def run_ours(args, world, rank, local):
                 "traffic": traffic, "algorithmic_bytes_per_launch": STEP_BYTES_MASTER * N,
                 "kernel_ms": round(step_kernel_ms, 5), "kernel_ms_samples": len(sample)}
 
+    roofline["frac_of_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
     if args.quick:
         variants, e2e = None, None
     else:
+        ceiling = copy_ceiling(STEP_BYTES_MASTER // 2 * N, stream, device)
+        ceiling["step_kernel_frac"] = round(achieved / ceiling["gbs"], 4)
+        roofline["copy_ceiling"] = ceiling
         variants = measure_variants(mp, st, grads[0], opt, N, entries, tab, stream, device, peak)
         e2e = measure_e2e(mp, st, grads[0], opt, N, stream, device, kw, min(args.steps, 200), step_no)
 
@@ -303,6 +308,21 @@ def time_events(fn, iters, stream):
         b.record(stream)
     torch.cuda.synchronize()
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def copy_ceiling(nbytes, stream, device, cap=1 << 32):
+    """A plain device-to-device copy (cudaMemcpyAsync, through torch's
+    copy_) moving as many bytes as the step kernel reads and writes, or 4 GiB
+    each way at most: the practical ceiling of a stream that reads and writes
+    equal amounts."""
+    nbytes = min(nbytes, cap) // 16 * 16
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    ms = time_events(lambda: dst.copy_(src), 10, stream)
+    del src, dst
+    return {"gbs": round(2 * nbytes / ms / 1e6, 1), "bytes_each_way": nbytes,
+            "what": "device-to-device cudaMemcpyAsync, CUDA-event mean of 10"}
 
 
 def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
@@ -419,6 +439,8 @@ class OracleSample:
 
 
 def cpu_baseline(seconds):
+    """The oracle on a prefix of the set: single-threaded (the reported
+    value), and on every host core (`all_cores`)."""
     n = 1 << 22
     s = OracleSample(n)
     s.step()
@@ -428,9 +450,53 @@ def cpu_baseline(seconds):
         s.step()
         steps += 1
     dt = time.perf_counter() - t0
-    return {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"first {n} params of the GPT-2 124M set, {steps} steps (norm + AdamW + SR), "
-                      f"{dt:.1f} s, single-threaded C oracle"}
+    out = {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"first {n} params of the GPT-2 124M set, {steps} steps (norm + AdamW + SR), "
+                     f"{dt:.1f} s, single-threaded C oracle"}
+    out["all_cores"] = cpu_baseline_all_cores(seconds)
+    return out
+
+
+def cpu_baseline_all_cores(seconds, n=1 << 24):
+    """The same oracle on every host core: the norm as it stands (one thread,
+    one sequential sum), then the step over contiguous shards, one thread
+    each. Sharding the step changes no result (every element is independent
+    given the scale), and the C calls release the GIL, so the shards run in
+    parallel."""
+    import threading
+    cores = os.cpu_count() or 1
+    s = OracleSample(n)
+    per = ((n + cores - 1) // cores + 7) // 8 * 8
+    bounds = [(a, min(n, a + per)) for a in range(0, n, per)]
+    H = W.HYPER
+
+    def step():
+        s.t += 1
+        g = s.grads[s.t % 2]
+        _, _, scale = s.oracle.grad_norm(g, H["clip"])
+        status = []
+
+        def shard(a, b):
+            status.append(s.oracle.adamw_step(
+                s.params[a:b], g[a:b], s.master[a:b], s.m[a:b], s.v[a:b], a, s.tab, H["lr"], H["beta1"],
+                H["beta2"], H["eps"], H["weight_decay"], float(scale), s.t, W.step_seed(s.t)))
+        threads = [threading.Thread(target=shard, args=ab) for ab in bounds]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        assert status == [0] * len(bounds)
+
+    step()
+    t0 = time.perf_counter()
+    steps = 0
+    while time.perf_counter() - t0 < seconds:
+        step()
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": len(bounds), "kind": "oracle",
+            "sample": f"first {n} params of the GPT-2 124M set, {steps} steps, {dt:.1f} s: norm on one thread, "
+                      f"step on {len(bounds)} threads over contiguous shards"}
 
 
 def run_reference(args, world, rank):
