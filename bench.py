@@ -133,7 +133,7 @@ def profiled_traffic_bytes():
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     if not m or not h or h.group(1) != kernel_source_hash():
         return None
-    return float(m.group(1))
+    return int(float(m.group(1)))
 
 
 class ClockSampler:
@@ -246,7 +246,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
-    step_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in sample.values())
+    step_kernel_times = [a.elapsed_time(b) for a, b in sample.values()]
+    step_kernel_ms = statistics.mean(step_kernel_times)
     opt.check_status()
     max_s = max_over_ranks(total_ms / 1e3, world, device)
     value = whole_job_value(N, world, args.steps, max_s)
@@ -258,7 +259,9 @@ def run_ours(args, world, rank, local):
     roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master>", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": traffic, "algorithmic_bytes_per_launch": STEP_BYTES_MASTER * N,
-                "kernel_ms": round(step_kernel_ms, 5), "kernel_ms_samples": len(sample)}
+                "kernel_ms": round(step_kernel_ms, 5), "kernel_ms_samples": len(sample),
+                "kernel_ms_median": round(statistics.median(step_kernel_times), 5),
+                "kernel_ms_min": round(min(step_kernel_times), 5)}
 
     roofline["frac_of_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
     if args.quick:
@@ -298,7 +301,12 @@ def run_ours(args, world, rank, local):
     return line
 
 
+LAST_TIMING = {}
+
+
 def time_events(fn, iters, stream):
+    """Mean CUDA-event time of fn over `iters` launches after one warm-up;
+    the median and minimum are left in LAST_TIMING."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     fn()
     torch.cuda.synchronize()
@@ -307,7 +315,10 @@ def time_events(fn, iters, stream):
         fn()
         b.record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    times = [a.elapsed_time(b) for a, b in evs]
+    LAST_TIMING.clear()
+    LAST_TIMING.update(ms_median=round(statistics.median(times), 5), ms_min=round(min(times), 5), launches=iters)
+    return statistics.mean(times)
 
 
 def copy_ceiling(nbytes, stream, device, cap=1 << 32):
@@ -332,22 +343,45 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     iters = 20
     ms = time_events(lambda: mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N,
                                              stream=stream), iters, stream)
-    out["grad_norm"] = {"ms": round(ms, 5), "gbs": round(NORM_BYTES * N / ms / 1e6, 1),
+    out["grad_norm"] = {**LAST_TIMING, "ms": round(ms, 5), "gbs": round(NORM_BYTES * N / ms / 1e6, 1),
                         "frac": round(NORM_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_param": NORM_BYTES}
     # no-master variant, in place on params, m, v (no extra copy: the
     # Llama-3-8B state alone is 128 GB)
     ms = time_events(lambda: mp.mp_adamw_step(st["params"], g, None, st["m"], st["v"], opt.table,
                                               d_grad_scale=opt.d_scale, t=5, seed=5, n=N, stream=stream, **kw),
                      iters, stream)
-    out["step_no_master"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+    out["step_no_master"] = {**LAST_TIMING, "ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
                              "gbs": round(STEP_BYTES_NOMASTER * N / ms / 1e6, 1),
                              "frac": round(STEP_BYTES_NOMASTER * N / ms / 1e6 / peak, 4),
                              "bytes_per_param": STEP_BYTES_NOMASTER}
     ms = time_events(lambda: mp.mp_stochastic_round(st["params"], st["master"], 7, n=N, stream=stream), iters,
                      stream)
-    out["stochastic_round"] = {"ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
+    out["stochastic_round"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
                                "gbs": round(SR_BYTES * N / ms / 1e6, 1),
                                "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
+    # The whole step as one captured CUDA graph (mp_optimizer_step_graph: the
+    # step count lives on the device), replayed once per step.
+    opt.init_device_clock(t=1000, seed_base=W.BASE_SEED)
+    opt.step_graph(st["params"], g, st["master"], st["m"], st["v"], stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt.step_graph(st["params"], g, st["master"], st["m"], st["v"])
+    reps = max(iters, 200 if N < (1 << 24) else iters)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    opt.check_status()
+    out["graph_step"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+                         "gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N / ms / 1e6, 1), "replays": reps,
+                         "what": "norm + AdamW + SR as one CUDA graph, replayed back to back (one event pair)"}
+    del graph
     per = N // 8
 
     def shards():
@@ -357,7 +391,7 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
                              d_grad_scale=opt.d_scale, t=6, seed=6, global_offset=r * per, n=per, stream=stream,
                              **kw)
     ms = time_events(shards, iters // 2, stream)
-    out["step_8_shards"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+    out["step_8_shards"] = {**LAST_TIMING, "ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
                             "gbs": round(STEP_BYTES_MASTER * N / ms / 1e6, 1), "launches": 8}
     return out
 

@@ -283,6 +283,88 @@ int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_gr
                       float* host_norm, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Replayable steps: the step count on the device.
+ *
+ * mp_optimizer_step bakes t, seed and lr into its launches, so a recorded
+ * launch sequence (a CUDA graph captured from a stream) would repeat one
+ * step. mp_optimizer_step_graph reads them from device memory instead: the
+ * norm's finalize kernel advances a device step counter and looks up that
+ * step's bias corrections in a device table, and the update kernel reads
+ * them from there. One capture then serves every later step, with no host
+ * work per step. The arithmetic is mp_optimizer_step's: the same kernels'
+ * per-element code, the same bias corrections (the table holds the values
+ * the host computes for mp_adamw_step, [LLMC] §2.2 m_hat/v_hat and §4
+ * t = step + 1; [CMU13] §1.7 the factor 1 - beta^t), so a run of graph steps
+ * is bit-identical to the same run of mp_optimizer_step calls.
+ *
+ * The step state (device memory, 32 B, 16-B aligned, owned by the caller):
+ *   t          steps taken so far (0 before the first). Each call adds 1 and
+ *              updates with the new t. Set it to resume from a checkpoint.
+ *   seed_base  step t rounds with seed = seed_base + t (mod 2^32).
+ *   lr         learning rate of the next step; the caller may write it
+ *              between steps (a schedule).
+ *   seed, bc1, bc2   written by each call: the seed and bias corrections of
+ *              the step it took.
+ * ------------------------------------------------------------------------- */
+typedef struct mp_step_state {
+    int32_t t;
+    uint32_t seed_base;
+    float lr;
+    uint32_t reserved0; /* 0 */
+    uint32_t seed;
+    float bc1, bc2;
+    uint32_t reserved1; /* 0 */
+} mp_step_state_t;
+
+/* Length of the bias-correction table for (beta1, beta2): the first step t at
+ * which both (float)(1 - beta^t) round to exactly 1.0f. Every later step has
+ * the same corrections, so a table of this length serves every t. Returns 0
+ * if beta1 or beta2 is outside [0, 1) or the length would exceed 2^26
+ * entries (beta within ~2^-22 of 1). Host only; no CUDA call. */
+int64_t mp_bias_table_len(float beta1, float beta2);
+
+/* Fills out[2*(t-1)] = bc1(t), out[2*(t-1)+1] = bc2(t) for t = 1..len, with
+ * bc(t) = (float)(1 - beta^t) computed in double exactly as mp_adamw_step's
+ * host side does. `out` is HOST memory of 2*len floats; copy it to the
+ * device for mp_optimizer_step_graph. Host only; no CUDA call.
+ * Errors: MP_ERR_NULL, MP_ERR_RANGE (betas outside [0, 1), len < 1). */
+int mp_bias_table(float beta1, float beta2, int64_t len, float* out);
+
+/* ---------------------------------------------------------------------------
+ * The whole step, replayable (see above). Enqueues the same kernels as
+ * mp_optimizer_step; per call, on the device and in stream order:
+ *   t = d_state->t + 1;  seed = d_state->seed_base + t;
+ *   (bc1, bc2) = d_bias[min(t, bias_len) - 1];  lr = d_state->lr;
+ *   then the norm, the optional outlier check and the update with those.
+ * t advances on every call, also when the update is refused or skipped
+ * (the train loop's step count moves on regardless, [LLMC] §4).
+ *
+ *   d_state      mp_step_state_t, device, 16-B aligned, read and written.
+ *   d_bias       float[2*bias_len], device: mp_bias_table's contents for
+ *                these betas; read only.
+ *   bias_len     >= 1. If a step's t exceeds bias_len while the last entry
+ *                is not (1.0f, 1.0f), or d_state->t is negative or already
+ *                2^31 - 1, the step is refused on the device: nothing is
+ *                written, t does not advance and *d_status gets MP_ERR_RANGE
+ *                (if it held 0).
+ *   hyper        as mp_optimizer_step; hyper->lr is not used (d_state->lr is).
+ * Every other argument as mp_optimizer_step, and the same host-side checks.
+ * Capture: make one call (a real step) before capturing, so the library's
+ * per-device lookups are done; a capture records the pointers and n, so the
+ * recorded graph must be replayed with those same buffers.
+ * Errors: as mp_optimizer_step.
+ * ------------------------------------------------------------------------- */
+int mp_optimizer_step_graph(uint16_t* params, uint16_t* grads, const uint16_t* host_grads,
+                            float* master, float* m, float* v, uint64_t n,
+                            const mp_tensor_t* table, int32_t n_tensors,
+                            const mp_hyper_t* hyper, mp_step_state_t* d_state,
+                            const float* d_bias, int64_t bias_len,
+                            void* workspace, size_t workspace_bytes,
+                            void* outlier_state, float outlier_z, double* d_z,
+                            float* d_norm, float* d_scale, int32_t* d_status,
+                            float* host_norm, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Gradient norm without a workspace. The pages have no counterpart to this
  * call: it exists for callers that cannot allocate device memory — a host
  * framework that reserves all device memory in its own pool and hands a

@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from contextlib import nullcontext as _nullcontext
 from typing import Iterable, Optional, Sequence, Tuple
 
 import torch
@@ -47,6 +48,13 @@ class MpTensor(ctypes.Structure):
 class MpHyper(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("clip", ctypes.c_float)]
+
+
+class MpStepState(ctypes.Structure):
+    """mp_step_state_t: the device step counter of replayable steps (32 B)."""
+    _fields_ = [("t", ctypes.c_int32), ("seed_base", ctypes.c_uint32), ("lr", ctypes.c_float),
+                ("reserved0", ctypes.c_uint32), ("seed", ctypes.c_uint32), ("bc1", ctypes.c_float),
+                ("bc2", ctypes.c_float), ("reserved1", ctypes.c_uint32)]
 
 
 def _load():
@@ -85,6 +93,14 @@ def _load():
                                     vp, vp, vp, vp, vp]
     L.mp_grad_norm_noalloc.restype = ctypes.c_int
     L.mp_grad_norm_noalloc.argtypes = [vp, u64, f32, vp, vp, vp, vp]
+    L.mp_bias_table_len.restype = ctypes.c_int64
+    L.mp_bias_table_len.argtypes = [f32, f32]
+    L.mp_bias_table.restype = ctypes.c_int
+    L.mp_bias_table.argtypes = [f32, f32, ctypes.c_int64, vp]
+    L.mp_optimizer_step_graph.restype = ctypes.c_int
+    L.mp_optimizer_step_graph.argtypes = [vp, vp, vp, vp, vp, vp, u64, ctypes.POINTER(MpTensor), i32,
+                                          ctypes.POINTER(MpHyper), vp, vp, ctypes.c_int64, vp, ctypes.c_size_t,
+                                          vp, f32, vp, vp, vp, vp, vp, vp]
     return L
 
 
@@ -263,6 +279,49 @@ def mp_optimizer_step(params: torch.Tensor, grads: torch.Tensor, master: Optiona
     _check(st, "mp_optimizer_step")
 
 
+def mp_bias_table_len(beta1: float, beta2: float) -> int:
+    """Entries the bias-correction table needs (0: betas out of range)."""
+    return int(_lib.mp_bias_table_len(beta1, beta2))
+
+
+def mp_bias_table(beta1: float, beta2: float, length: Optional[int] = None) -> torch.Tensor:
+    """The host-computed bias corrections (bc1(t), bc2(t)) for t = 1..length
+    as a CPU float32 tensor of 2*length values (mp_bias_table)."""
+    length = mp_bias_table_len(beta1, beta2) if length is None else length
+    out = torch.empty(2 * max(1, length), dtype=torch.float32)
+    _check(_lib.mp_bias_table(beta1, beta2, length, out.data_ptr()), "mp_bias_table")
+    return out
+
+
+def mp_optimizer_step_graph(params: torch.Tensor, grads: torch.Tensor, master: Optional[torch.Tensor],
+                            m: torch.Tensor, v: torch.Tensor, table: "TensorTable", hyper: MpHyper, *,
+                            d_state: torch.Tensor, d_bias: torch.Tensor, workspace: torch.Tensor,
+                            d_norm: torch.Tensor, d_scale: torch.Tensor, d_status: Optional[torch.Tensor] = None,
+                            outlier_state: Optional[torch.Tensor] = None, outlier_z: float = 0.0,
+                            d_z: Optional[torch.Tensor] = None, host_grads: Optional[torch.Tensor] = None,
+                            host_norm: Optional[torch.Tensor] = None, n: Optional[int] = None,
+                            stream=None) -> None:
+    """mp_optimizer_step with t, seed and lr taken from the device step state
+    (d_state: 32 bytes of device memory holding an mp_step_state_t), so one
+    captured CUDA graph of this call serves every later step."""
+    n = m.numel() if n is None else n
+    if d_state.numel() * d_state.element_size() < ctypes.sizeof(MpStepState):
+        raise ValueError("d_state: smaller than mp_step_state_t")
+    st = _lib.mp_optimizer_step_graph(
+        _ptr(params, _BF16_LIKE, "params", n), _ptr(grads, _BF16_LIKE, "grads", n),
+        _host_ptr(host_grads, _BF16_LIKE, "host_grads", n),
+        _ptr(master, (torch.float32,), "master", n), _ptr(m, (torch.float32,), "m", n),
+        _ptr(v, (torch.float32,), "v", n), n, table.ctypes_array, table.n_tensors, ctypes.byref(hyper),
+        _ptr(d_state, (torch.uint8, torch.int32), "d_state"), _ptr(d_bias, (torch.float32,), "d_bias", 2),
+        d_bias.numel() // 2, _ptr(workspace, (torch.uint8, torch.float64, torch.int64), "workspace"),
+        workspace.numel() * workspace.element_size(),
+        _ptr(outlier_state, (torch.uint8, torch.float64), "outlier_state"), outlier_z,
+        _ptr(d_z, (torch.float64,), "d_z", 1), _ptr(d_norm, (torch.float32,), "d_norm", 1),
+        _ptr(d_scale, (torch.float32,), "d_scale", 1), _ptr(d_status, (torch.int32,), "d_status", 1),
+        _host_ptr(host_norm, (torch.float32,), "host_norm", 1), _stream(stream))
+    _check(st, "mp_optimizer_step_graph")
+
+
 def mp_outlier_state_bytes() -> int:
     return int(_lib.mp_outlier_state_bytes())
 
@@ -336,6 +395,47 @@ class Optimizer:
                           d_z=self.outlier.d_z if self.outlier is not None else None,
                           host_grads=host_grads, host_norm=host_norm, n=self.n, stream=stream)
 
+    # --- replayable steps: the step count lives on the device -------------
+    def init_device_clock(self, t: int = 0, seed_base: int = 0, lr: Optional[float] = None, stream=None):
+        """Creates the device step state (t = steps already taken, step t
+        rounds with seed seed_base + t) and the bias-correction table for
+        this optimizer's betas; step_graph() then needs no per-step host
+        arguments. Call again to reset or resume."""
+        st = MpStepState(int(t), int(seed_base) & 0xFFFFFFFF, float(self.hyper["lr"] if lr is None else lr),
+                         0, 0, 0.0, 0.0, 0)
+        raw = torch.frombuffer(bytearray(ctypes.string_at(ctypes.addressof(st), ctypes.sizeof(st))),
+                               dtype=torch.int32)
+        dev = self.d_norm.device
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            if getattr(self, "d_state", None) is None:
+                self.d_state = torch.empty(8, dtype=torch.int32, device=dev)
+                self.d_bias = mp_bias_table(self.hyper["beta1"], self.hyper["beta2"]).to(dev)
+            self.d_state.copy_(raw)
+
+    def set_lr(self, lr: float, stream=None):
+        """Stream-ordered write of the next steps' learning rate into the
+        device step state (between replays of a captured step)."""
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            self.d_state[2:3].view(torch.float32).fill_(float(lr))
+
+    def device_clock(self) -> dict:
+        """The device step state (synchronises): t, seed_base, lr, and the
+        seed and bias corrections of the last step taken."""
+        raw = self.d_state.cpu().numpy().tobytes()
+        st = MpStepState.from_buffer_copy(raw)
+        return dict(t=st.t, seed_base=st.seed_base, lr=st.lr, seed=st.seed, bc1=st.bc1, bc2=st.bc2)
+
+    def step_graph(self, params, grads, master, m, v, host_grads=None, host_norm=None, stream=None):
+        """One mp_optimizer_step_graph call: the next step of the device
+        clock. Capturable: record it once in a CUDA graph and replay it."""
+        mp_optimizer_step_graph(params, grads, master, m, v, self.table, self.hyper_struct, d_state=self.d_state,
+                                d_bias=self.d_bias, workspace=self.workspace, d_norm=self.d_norm,
+                                d_scale=self.d_scale, d_status=self.d_status,
+                                outlier_state=self.outlier.state if self.outlier is not None else None,
+                                outlier_z=self.outlier.z_threshold if self.outlier is not None else 0.0,
+                                d_z=self.outlier.d_z if self.outlier is not None else None,
+                                host_grads=host_grads, host_norm=host_norm, n=self.n, stream=stream)
+
     def take_status(self) -> int:
         """Device status of the steps since the last call (0, MP_ERR_NONFINITE
         or MP_SKIPPED_OUTLIER; the first one recorded wins); clears it."""
@@ -354,5 +454,6 @@ __all__ = [
     "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "OutlierDetector", "lib", "abi_version",
     "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
-    "mp_stochastic_round", "mp_noise_u32", "LIB_PATH",
+    "mp_stochastic_round", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
+    "MpStepState", "LIB_PATH",
 ]

@@ -21,6 +21,16 @@ int cuda_fail(cudaError_t e) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Bias correction 1 - beta^t of step t, in double, rounded once to float.
+// mp_adamw_step and the device table of replayable steps both use this.
+float bias_correction(float beta, int64_t t) {
+  return static_cast<float>(1.0 - std::pow(static_cast<double>(beta), static_cast<double>(t)));
+}
+
+bool beta_ok(float beta) { return beta >= 0.0f && beta < 1.0f; }
+
+constexpr int64_t kMaxBiasLen = int64_t{1} << 26;
+
 }  // namespace
 
 namespace mpk {
@@ -160,8 +170,8 @@ int plan_step(uint16_t* params, const uint16_t* grads, float* master, float* m, 
   base.beta2 = beta2;
   base.eps = eps;
   base.wd = weight_decay;
-  base.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), static_cast<double>(t)));
-  base.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), static_cast<double>(t)));
+  base.bc1 = bias_correction(beta1, t);
+  base.bc2 = bias_correction(beta2, t);
   base.seed = seed;
   plan->vec = aligned(params, 8) && aligned(grads, 8) && aligned(master, 16) && aligned(m, 16) && aligned(v, 16);
   return MP_OK;
@@ -230,11 +240,19 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master, float*
   return MP_OK;
 }
 
-int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads, float* master, float* m,
-                      float* v, uint64_t n, const mp_tensor_t* table, int32_t n_tensors, const mp_hyper_t* hyper,
-                      int32_t t, uint32_t seed, void* workspace, size_t workspace_bytes, void* outlier_state,
-                      float outlier_z, double* d_z, float* d_norm, float* d_scale, int32_t* d_status,
-                      float* host_norm, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// mp_optimizer_step and mp_optimizer_step_graph: with `clock`, the norm's
+// finalize kernel advances the device step counter and the update reads lr,
+// seed and bias corrections from the device state (t, seed and hyper->lr are
+// then unused).
+int optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads, float* master, float* m,
+                   float* v, uint64_t n, const mp_tensor_t* table, int32_t n_tensors, const mp_hyper_t* hyper,
+                   int32_t t, uint32_t seed, const mpk::StepClock* clock, void* workspace, size_t workspace_bytes,
+                   void* outlier_state, float outlier_z, double* d_z, float* d_norm, float* d_scale,
+                   int32_t* d_status, float* host_norm, void* stream) {
   if (hyper == nullptr || d_norm == nullptr || d_scale == nullptr) return MP_ERR_NULL;
   if (workspace == nullptr) return MP_ERR_WORKSPACE;
   if (!aligned(workspace, 8) || !aligned(d_norm, 4) || !aligned(d_scale, 4) || !aligned(outlier_state, 8) ||
@@ -243,9 +261,11 @@ int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_gr
   if (!(hyper->clip > 0.0f) || !std::isfinite(hyper->clip)) return MP_ERR_RANGE;
   StepPlan plan;
   if (n != 0) {
-    const int st = plan_step(params, grads, master, m, v, 0, n, table, n_tensors, hyper->lr, hyper->beta1,
+    const float lr = clock != nullptr ? 0.0f : hyper->lr;
+    const int st = plan_step(params, grads, master, m, v, 0, n, table, n_tensors, lr, hyper->beta1,
                              hyper->beta2, hyper->eps, hyper->weight_decay, d_scale, t, seed, d_status, &plan);
     if (st != MP_OK) return st;
+    if (clock != nullptr) plan.base.dstate = clock->state;
   }
   // Host gradients must be page-locked: their device-visible address is read
   // by the norm kernel, which also writes the device copy into `grads`.
@@ -269,7 +289,7 @@ int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_gr
   if (workspace_bytes < sizeof(double) * static_cast<size_t>(nb)) return MP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = mpk::launch_norm(src, n, vec, static_cast<double*>(workspace), nb, hyper->clip, d_norm, d_scale, nullptr,
-                       s, copy ? grads : nullptr);
+                       s, copy ? grads : nullptr, clock);
   if (e == cudaSuccess && outlier_state != nullptr)
     e = mpk::launch_outlier_check(outlier_state, d_norm, outlier_z, d_scale, d_z, d_status, s);
   if (e == cudaSuccess && n != 0) e = launch_step(plan, params, grads, master, m, v, dev, s);
@@ -277,6 +297,52 @@ int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_gr
     e = cudaMemcpyAsync(host_norm, d_norm, sizeof(float), cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return MP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads, float* master, float* m,
+                      float* v, uint64_t n, const mp_tensor_t* table, int32_t n_tensors, const mp_hyper_t* hyper,
+                      int32_t t, uint32_t seed, void* workspace, size_t workspace_bytes, void* outlier_state,
+                      float outlier_z, double* d_z, float* d_norm, float* d_scale, int32_t* d_status,
+                      float* host_norm, void* stream) {
+  return optimizer_step(params, grads, host_grads, master, m, v, n, table, n_tensors, hyper, t, seed, nullptr,
+                        workspace, workspace_bytes, outlier_state, outlier_z, d_z, d_norm, d_scale, d_status,
+                        host_norm, stream);
+}
+
+int64_t mp_bias_table_len(float beta1, float beta2) {
+  if (!beta_ok(beta1) || !beta_ok(beta2)) return 0;
+  for (int64_t t = 1; t <= kMaxBiasLen; ++t)
+    if (bias_correction(beta1, t) == 1.0f && bias_correction(beta2, t) == 1.0f) return t;
+  return 0;
+}
+
+int mp_bias_table(float beta1, float beta2, int64_t len, float* out) {
+  if (out == nullptr) return MP_ERR_NULL;
+  if (!beta_ok(beta1) || !beta_ok(beta2) || len < 1 || len > kMaxBiasLen) return MP_ERR_RANGE;
+  for (int64_t t = 1; t <= len; ++t) {
+    out[2 * (t - 1)] = bias_correction(beta1, t);
+    out[2 * (t - 1) + 1] = bias_correction(beta2, t);
+  }
+  return MP_OK;
+}
+
+int mp_optimizer_step_graph(uint16_t* params, uint16_t* grads, const uint16_t* host_grads, float* master,
+                            float* m, float* v, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                            const mp_hyper_t* hyper, mp_step_state_t* d_state, const float* d_bias,
+                            int64_t bias_len, void* workspace, size_t workspace_bytes, void* outlier_state,
+                            float outlier_z, double* d_z, float* d_norm, float* d_scale, int32_t* d_status,
+                            float* host_norm, void* stream) {
+  if (d_state == nullptr || d_bias == nullptr) return MP_ERR_NULL;
+  if (!aligned(d_state, 16) || !aligned(d_bias, 4)) return MP_ERR_ALIGN;
+  if (bias_len < 1 || bias_len > kMaxBiasLen) return MP_ERR_RANGE;
+  const mpk::StepClock clock{d_state, d_bias, bias_len, d_status};
+  return optimizer_step(params, grads, host_grads, master, m, v, n, table, n_tensors, hyper, 1, 0, &clock,
+                        workspace, workspace_bytes, outlier_state, outlier_z, d_z, d_norm, d_scale, d_status,
+                        host_norm, stream);
 }
 
 int mp_stochastic_round(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n, uint32_t seed,

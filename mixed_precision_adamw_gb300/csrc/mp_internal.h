@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "mp_adamw.h"
+
 namespace mpk {
 
 // Decay segments: maximal runs of consecutive elements with the same decay
@@ -30,6 +32,21 @@ struct StepArgs {
   uint32_t seed;
   uint32_t nseg;         // segments covering [goff, goff + n)
   uint32_t first_decay;  // decay flag of segment 0; flags alternate after it
+  // Non-null: lr, bc1, bc2 and seed are read from this device state (written
+  // by the norm's finalize kernel earlier in the stream) instead of the
+  // fields above.
+  const mp_step_state_t* dstate;
+};
+
+// The device step counter of a replayable step (mp_optimizer_step_graph):
+// the norm's finalize kernel advances state->t and writes that step's seed
+// and bias corrections (bias[2(t-1)], bias[2(t-1)+1], clamped to the last
+// entry) into the state for the update kernel.
+struct StepClock {
+  mp_step_state_t* state;  // nullptr: no device step counter
+  const float* bias;
+  int64_t bias_len;
+  int32_t* d_status;       // may be nullptr
 };
 
 // Launches a kernel with programmatic dependent launch allowed (the kernel
@@ -67,9 +84,11 @@ cudaError_t launch_adamw(const StepArgs& a, const uint64_t* seg_end, bool vec,
 int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev);
 // copy_out != nullptr: grads may be page-locked host memory (device-visible
 // address); the kernel also writes every gradient to copy_out (device).
+// clock != nullptr: the finalize kernel also advances the device step counter.
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials,
                         int nblocks, float clip, float* d_norm, float* d_scale,
-                        double* d_sumsq, cudaStream_t stream, uint16_t* copy_out = nullptr);
+                        double* d_sumsq, cudaStream_t stream, uint16_t* copy_out = nullptr,
+                        const StepClock* clock = nullptr);
 
 // Outlier check of the grad norm (mp_outlier.cu): d_state holds the window.
 cudaError_t launch_outlier_check(void* d_state, const float* d_norm, float z_threshold, float* d_scale,

@@ -137,9 +137,28 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
   if (threadIdx.x == 0) partials[blockIdx.x] = S;
 }
 
+// Advances the device step counter (one thread). Returns false, leaving the
+// state untouched, when the step cannot be taken: a negative or saturated
+// count, or a t beyond a bias table whose last entry is not (1, 1).
+__device__ __forceinline__ bool advance_clock(const StepClock& c) {
+  mp_step_state_t* st = c.state;
+  const int32_t t0 = st->t;
+  if (t0 < 0 || t0 == 0x7FFFFFFF) return false;
+  const int32_t t = t0 + 1;
+  const int64_t last = c.bias_len - 1;
+  const int64_t k = (static_cast<int64_t>(t) - 1 < last) ? static_cast<int64_t>(t) - 1 : last;
+  const float bc1 = c.bias[2 * k], bc2 = c.bias[2 * k + 1];
+  if (static_cast<int64_t>(t) - 1 > last && !(bc1 == 1.0f && bc2 == 1.0f)) return false;
+  st->t = t;
+  st->seed = st->seed_base + static_cast<uint32_t>(t);
+  st->bc1 = bc1;
+  st->bc2 = bc2;
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads)
 norm_finalize_kernel(const double* __restrict__ partials, int nb, float clip,
-                     float* d_norm, float* d_scale, double* d_sumsq) {
+                     float* d_norm, float* d_scale, double* d_sumsq, const StepClock clock) {
   __shared__ double sh[kThreads / 32 + 1];
   pdl_enter();
   double d = 0.0;
@@ -153,6 +172,10 @@ norm_finalize_kernel(const double* __restrict__ partials, int nb, float clip,
     } else {
       const float q = __fdiv_rn(clip, norm);  // norm == 0 gives +Inf -> 1
       scale = q < 1.0f ? q : 1.0f;
+    }
+    if (clock.state != nullptr && !advance_clock(clock)) {
+      scale = __int_as_float(0x7FC00000);
+      if (clock.d_status != nullptr) atomicCAS(clock.d_status, 0, MP_ERR_RANGE);
     }
     *d_norm = norm;
     *d_scale = scale;
@@ -173,7 +196,8 @@ int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev) {
 
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials, int nblocks,
                         float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream,
-                        uint16_t* copy_out) {
+                        uint16_t* copy_out, const StepClock* clock) {
+  const StepClock c = clock != nullptr ? *clock : StepClock{nullptr, nullptr, 0, nullptr};
   cudaError_t e = copy_out == nullptr
                       ? launch_pdl(norm_partial_kernel<false>, static_cast<unsigned>(nblocks), kThreads, stream,
                                    grads, n, vec ? 1 : 0, partials, copy_out)
@@ -181,7 +205,7 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
                                    grads, n, vec ? 1 : 0, partials, copy_out);
   if (e != cudaSuccess) return e;
   return launch_pdl(norm_finalize_kernel, 1u, kThreads, stream, static_cast<const double*>(partials), nblocks,
-                    clip, d_norm, d_scale, d_sumsq);
+                    clip, d_norm, d_scale, d_sumsq, c);
 }
 
 }  // namespace mpk

@@ -68,8 +68,20 @@ __device__ __forceinline__ void group_decay(Cursor& c, const SegTable<CAP>& t, c
   }
 }
 
-__device__ __forceinline__ Hyper hyper_of(const StepArgs& p) {
-  return Hyper{p.lr, p.beta1, p.beta2, p.eps, p.wd, p.bc1, p.bc2};
+// The launch's hyperparameters and rounding seed; with kDev, the per-step
+// ones (lr, bias corrections, seed) come from the device step state.
+template <bool kDev>
+__device__ __forceinline__ Hyper step_scalars(const StepArgs& p, uint32_t& seed) {
+  Hyper h{p.lr, p.beta1, p.beta2, p.eps, p.wd, p.bc1, p.bc2};
+  seed = p.seed;
+  if (kDev) {
+    const mp_step_state_t* s = p.dstate;
+    h.lr = s->lr;
+    h.bc1 = s->bc1;
+    h.bc2 = s->bc2;
+    seed = s->seed;
+  }
+  return h;
 }
 
 // Updates 4 consecutive elements starting at global index gi.
@@ -93,7 +105,7 @@ __device__ __forceinline__ uint2 group_update(uint2 graw, float4& m4, float4& v4
 
 template <bool kMaster, uint32_t CAP>
 __device__ __forceinline__ void elem_update(const StepArgs& p, const SegTable<CAP>& t, Cursor& c,
-                                            uint64_t i, float scale, const Hyper& h) {
+                                            uint64_t i, float scale, const Hyper& h, uint32_t seed) {
   const uint64_t gi = p.goff + i;
   seek(c, t, gi);
   float m = p.m[i];
@@ -103,7 +115,7 @@ __device__ __forceinline__ void elem_update(const StepArgs& p, const SegTable<CA
   p.m[i] = m;
   p.v[i] = v;
   if (kMaster) p.master[i] = w;
-  p.params[i] = static_cast<uint16_t>(sr_bf16_c(w, draw16_complement(noise_pos(gi), p.seed)));
+  p.params[i] = static_cast<uint16_t>(sr_bf16_c(w, draw16_complement(noise_pos(gi), seed)));
 }
 
 // Reads the clip scale; a non-finite scale stops every thread before any
@@ -119,7 +131,7 @@ __device__ __forceinline__ bool read_scale(const StepArgs& p, float& scale) {
 }
 
 // Resident blocks per SM the vector kernel is compiled for: the with-master
-// kernel keeps 3 blocks of 256 threads (it compiles to 76 registers; forcing 4
+// kernel keeps 3 blocks of 256 threads (it compiles to 72 registers; forcing 4
 // blocks, i.e. at most 64 registers, was 8 % slower on GB300); the no-master
 // kernel moves fewer bytes per element and runs 9 % faster at 4 blocks (63
 // registers), where the extra warps hide more memory latency.
@@ -132,13 +144,14 @@ struct VecOccupancy {
 // Block-iteration k covers tile k of kTile elements; thread t handles the two
 // 4-element groups at tile offsets 4t and 4t + 4*kThreads, so every warp-wide
 // load or store is one contiguous 512-B (fp32) or 256-B (bf16) span.
-template <bool kMaster, uint32_t CAP>
+template <bool kMaster, uint32_t CAP, bool kDev>
 __global__ void __launch_bounds__(kThreads, VecOccupancy<kMaster>::kMinBlocks)
 adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ SegTable<CAP> segs) {
   pdl_enter();
   float scale;
   if (!read_scale(p, scale)) return;
-  const Hyper h = hyper_of(p);
+  uint32_t seed;
+  const Hyper h = step_scalars<kDev>(p, seed);
   const uint64_t ntiles = p.n / kTile;
   const uint64_t stride_tail = static_cast<uint64_t>(gridDim.x) * kThreads;
   const uint64_t tail0 = ntiles * kTile + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -174,8 +187,8 @@ adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Seg
     group_decay(c, segs, p, p.goff + e0, wd0);
     group_decay(c, segs, p, p.goff + e1, wd1);
 
-    const uint2 q0 = group_update(g0, m0, v0, w0, wd0, scale, h, p.goff + e0, p.seed);
-    const uint2 q1 = group_update(g1, m1, v1, w1, wd1, scale, h, p.goff + e1, p.seed);
+    const uint2 q0 = group_update(g0, m0, v0, w0, wd0, scale, h, p.goff + e0, seed);
+    const uint2 q1 = group_update(g1, m1, v1, w1, wd1, scale, h, p.goff + e1, seed);
 
     __stcs(reinterpret_cast<float4*>(p.m + e0), m0);
     __stcs(reinterpret_cast<float4*>(p.m + e1), m1);
@@ -189,23 +202,24 @@ adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Seg
     __stcs(reinterpret_cast<uint2*>(p.params + e1), q1);
   }
   // Ragged tail (< kTile elements), one element per thread.
-  for (uint64_t i = tail0; i < p.n; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h);
+  for (uint64_t i = tail0; i < p.n; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
 }
 
 // Scalar path for buffers that are not vector-aligned: same arithmetic.
-template <bool kMaster, uint32_t CAP>
+template <bool kMaster, uint32_t CAP, bool kDev>
 __global__ void __launch_bounds__(kThreads)
 adamw_scalar_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ SegTable<CAP> segs) {
   pdl_enter();
   float scale;
   if (!read_scale(p, scale)) return;
-  const Hyper h = hyper_of(p);
+  uint32_t seed;
+  const Hyper h = step_scalars<kDev>(p, seed);
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x;
   Cursor c;
   c.s = seg_find(segs, p.nseg, p.goff + (i < p.n ? i : p.n - 1));
   c.end = segs.end[c.s];
-  for (; i < p.n; i += stride) elem_update<kMaster>(p, segs, c, i, scale, h);
+  for (; i < p.n; i += stride) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
 }
 
 // Resident blocks per SM of `kernel` on `device`, queried once. `cache` must
@@ -222,23 +236,23 @@ int blocks_per_sm(K kernel, int device, int (&cache)[64]) {
   return nb;
 }
 
-template <bool kMaster, uint32_t CAP>
+template <bool kMaster, uint32_t CAP, bool kDev>
 cudaError_t launch_cap(const StepArgs& a, const uint64_t* seg_end, bool vec, const DeviceInfo& dev,
                        cudaStream_t stream) {
   SegTable<CAP> t;
   for (uint32_t s = 0; s < a.nseg; ++s) t.end[s] = seg_end[s];
   for (uint32_t s = a.nseg; s < CAP; ++s) t.end[s] = seg_end[a.nseg - 1];
-  static int vec_occupancy[64], scalar_occupancy[64];  // one cache per <kMaster, CAP> kernel
+  static int vec_occupancy[64], scalar_occupancy[64];  // one cache per <kMaster, CAP, kDev> kernel
   const uint64_t ntiles = a.n / kTile;
   if (vec) {
-    auto k = adamw_vec_kernel<kMaster, CAP>;
+    auto k = adamw_vec_kernel<kMaster, CAP, kDev>;
     const uint64_t cap = static_cast<uint64_t>(dev.sms) * blocks_per_sm(k, dev.device, vec_occupancy);
     uint64_t blocks = ntiles ? ntiles : (a.n + kThreads - 1) / kThreads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return launch_pdl(k, static_cast<unsigned>(blocks), kThreads, stream, a, t);
   } else {
-    auto k = adamw_scalar_kernel<kMaster, CAP>;
+    auto k = adamw_scalar_kernel<kMaster, CAP, kDev>;
     const uint64_t cap = static_cast<uint64_t>(dev.sms) * blocks_per_sm(k, dev.device, scalar_occupancy);
     uint64_t blocks = (a.n + kThreads - 1) / kThreads;
     if (blocks > cap) blocks = cap;
@@ -252,11 +266,14 @@ cudaError_t launch_cap(const StepArgs& a, const uint64_t* seg_end, bool vec, con
 cudaError_t launch_adamw(const StepArgs& a, const uint64_t* seg_end, bool vec, const DeviceInfo& dev,
                          cudaStream_t stream) {
   const bool master = a.master != nullptr;
+  if (a.dstate != nullptr)  // replayable steps: one segment capacity is enough
+    return master ? launch_cap<true, kSegCapLarge, true>(a, seg_end, vec, dev, stream)
+                  : launch_cap<false, kSegCapLarge, true>(a, seg_end, vec, dev, stream);
   if (a.nseg <= kSegCapSmall)
-    return master ? launch_cap<true, kSegCapSmall>(a, seg_end, vec, dev, stream)
-                  : launch_cap<false, kSegCapSmall>(a, seg_end, vec, dev, stream);
-  return master ? launch_cap<true, kSegCapLarge>(a, seg_end, vec, dev, stream)
-                : launch_cap<false, kSegCapLarge>(a, seg_end, vec, dev, stream);
+    return master ? launch_cap<true, kSegCapSmall, false>(a, seg_end, vec, dev, stream)
+                  : launch_cap<false, kSegCapSmall, false>(a, seg_end, vec, dev, stream);
+  return master ? launch_cap<true, kSegCapLarge, false>(a, seg_end, vec, dev, stream)
+                : launch_cap<false, kSegCapLarge, false>(a, seg_end, vec, dev, stream);
 }
 
 }  // namespace mpk

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -147,3 +148,59 @@ def test_optimizer_step_argument_checks(mp):
     assert call(host=FAKE + 1) == mp.MP_ERR_ALIGN
     assert call(n=101) == mp.MP_ERR_TABLE
     assert mp.status_string(mp.MP_ERR_ACCESS).startswith("MP_ERR_ACCESS")
+
+
+def test_graph_step_argument_checks(mp):
+    L = mp.lib()
+    tab = mp.TensorTable([(0, 100, 1)])
+    hyper = mp.MpHyper(float("nan"), 0.9, 0.95, 1e-8, 0.1, 1.0)  # lr is read from the device state
+
+    def call(**kw):
+        a = dict(params=FAKE, master=FAKE, n=100, state=FAKE, bias=FAKE, blen=338, norm=FAKE)
+        a.update(kw)
+        return L.mp_optimizer_step_graph(a["params"], FAKE, None, a["master"], FAKE, FAKE, a["n"],
+                                         tab.ctypes_array, tab.n_tensors, ctypes.byref(hyper), a["state"],
+                                         a["bias"], a["blen"], FAKE, 4096, None, 0.0, None, a["norm"], FAKE,
+                                         None, None, None)
+    assert call(state=None) == mp.MP_ERR_NULL
+    assert call(bias=None) == mp.MP_ERR_NULL
+    assert call(state=FAKE + 8) == mp.MP_ERR_ALIGN
+    assert call(bias=FAKE + 2) == mp.MP_ERR_ALIGN
+    assert call(blen=0) == mp.MP_ERR_RANGE
+    assert call(blen=(1 << 26) + 1) == mp.MP_ERR_RANGE
+    assert call(norm=None) == mp.MP_ERR_NULL
+    assert call(master=FAKE + 2) == mp.MP_ERR_ALIGN
+    assert call(n=101) == mp.MP_ERR_TABLE
+
+
+@pytest.mark.parametrize("b1,b2", [(0.9, 0.95), (0.9, 0.999), (0.8, 0.99), (0.0, 0.5), (0.0, 0.0),
+                                   (0.5, 0.9999)])
+def test_bias_table_matches_the_oracle(mp, b1, b2):
+    """The device table of replayable steps holds, for every t up to its
+    length, the bias corrections the oracle computes for step t, and its
+    last entry is the first (1, 1): every later step has the same values."""
+    import oracle
+    n = mp.mp_bias_table_len(b1, b2)
+    assert n >= 1
+    tab = mp.mp_bias_table(b1, b2).numpy()
+    assert tab.size == 2 * n
+    got = tab.view("u4").reshape(n, 2)
+    for t in range(1, n + 1):
+        bc1, bc2 = oracle.bias_corrections(b1, b2, t)
+        assert (int(got[t - 1, 0]), int(got[t - 1, 1])) == (
+            int(np.float32(bc1).view("u4")), int(np.float32(bc2).view("u4"))), t
+    assert tuple(tab[-2:]) == (1.0, 1.0)
+    if n > 1:
+        assert tuple(tab[-4:-2]) != (1.0, 1.0)
+    assert oracle.bias_corrections(b1, b2, n + 12345) == (1.0, 1.0)
+
+
+def test_bias_table_checks(mp):
+    L = mp.lib()
+    assert mp.mp_bias_table_len(1.0, 0.9) == 0
+    assert mp.mp_bias_table_len(0.9, -0.1) == 0
+    assert mp.mp_bias_table_len(0.9, float("nan")) == 0
+    assert mp.mp_bias_table_len(0.9, 1.0 - 2.0 ** -24) == 0  # would need more than 2^26 entries
+    assert L.mp_bias_table(0.9, 0.95, 4, None) == mp.MP_ERR_NULL
+    assert L.mp_bias_table(0.9, 0.95, 0, FAKE) == mp.MP_ERR_RANGE
+    assert L.mp_bias_table(1.0, 0.95, 4, FAKE) == mp.MP_ERR_RANGE
