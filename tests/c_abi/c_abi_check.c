@@ -5,8 +5,11 @@
  *
  * One optimizer step (mp_optimizer_step, then a second call of the pieces:
  * mp_grad_norm + mp_adamw_step) on n = 100,003 elements split into 7 tensors
- * with alternating decay flags, then mp_stochastic_round. Exit status 0 when
- * every output is bit-identical to the oracle's.
+ * with alternating decay flags, then mp_stochastic_round. Then steps 3-6 as
+ * replayable steps: step 3 a plain mp_optimizer_step_graph call, steps 4-6
+ * replays of one CUDA graph captured from a stream, with fresh gradients
+ * copied in between. Exit status 0 when every output is bit-identical to the
+ * oracle's.
  */
 #include <math.h>
 #include <stdint.h>
@@ -138,8 +141,80 @@ int main(void) {
     ok &= same(m, m_o, sizeof m, "m");
     ok &= same(v, v_o, sizeof v, "v");
     ok &= same(out_sr, out_sr_o, sizeof out_sr, "stochastic round");
-    printf("c_abi_check: %s (n=%u, norm %.7g, scale %.7g)\n", ok ? "bit-identical to the oracle" : "MISMATCH",
-           N, norm1, scale1);
+
+    /* steps 3..6 with the step count on the device: seed of step t = 10 + t */
+    enum { FIRST = 3, LAST = 6 };
+    static uint16_t grads_k[LAST - FIRST + 1][N];
+    float scales[LAST - FIRST + 1];
+    for (int k = 0; k <= LAST - FIRST; ++k)
+        for (uint32_t i = 0; i < N; ++i) grads_k[k][i] = to_bf16_bits((0.01f + 0.01f * (float)k) * rng_uniform());
+    const int64_t blen = mp_bias_table_len(hyper.beta1, hyper.beta2);
+    float* bias = (float*)malloc(sizeof(float) * 2 * (size_t)blen);
+    if (blen < 1 || bias == NULL) return 4;
+    MP(mp_bias_table(hyper.beta1, hyper.beta2, blen, bias));
+    float* d_bias;
+    mp_step_state_t* d_state;
+    CK(cudaMalloc((void**)&d_bias, sizeof(float) * 2 * (size_t)blen));
+    CK(cudaMalloc((void**)&d_state, sizeof(mp_step_state_t)));
+    CK(cudaMemcpy(d_bias, bias, sizeof(float) * 2 * (size_t)blen, cudaMemcpyHostToDevice));
+    const mp_step_state_t state0 = {FIRST - 1, 10u, hyper.lr, 0u, 0u, 0.0f, 0.0f, 0u};
+    CK(cudaMemcpy(d_state, &state0, sizeof state0, cudaMemcpyHostToDevice));
+    cudaStream_t stream;
+    CK(cudaStreamCreateWithFlags(&stream, cudaStreamNonBlocking));
+    cudaGraph_t graph = NULL;
+    cudaGraphExec_t exec = NULL;
+    for (int t = FIRST; t <= LAST; ++t) {
+        CK(cudaMemcpyAsync(d_grads, grads_k[t - FIRST], sizeof grads, cudaMemcpyHostToDevice, stream));
+        if (t == FIRST) { /* a plain call, then the capture of the same call */
+            MP(mp_optimizer_step_graph(d_params, d_grads, NULL, d_master, d_m, d_v, N, table, NT, &hyper, d_state,
+                                       d_bias, blen, d_ws, ws_bytes, NULL, 0.0f, NULL, d_norm, d_scale, d_status,
+                                       NULL, stream));
+            CK(cudaStreamSynchronize(stream));
+            CK(cudaStreamBeginCapture(stream, cudaStreamCaptureModeGlobal));
+            MP(mp_optimizer_step_graph(d_params, d_grads, NULL, d_master, d_m, d_v, N, table, NT, &hyper, d_state,
+                                       d_bias, blen, d_ws, ws_bytes, NULL, 0.0f, NULL, d_norm, d_scale, d_status,
+                                       NULL, stream));
+            CK(cudaStreamEndCapture(stream, &graph));
+            CK(cudaGraphInstantiate(&exec, graph, 0));
+        } else {
+            CK(cudaGraphLaunch(exec, stream));
+        }
+        CK(cudaMemcpyAsync(&scales[t - FIRST], d_scale, 4, cudaMemcpyDeviceToHost, stream));
+        CK(cudaStreamSynchronize(stream));
+    }
+    mp_step_state_t state;
+    CK(cudaMemcpy(&state, d_state, sizeof state, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(params, d_params, sizeof params, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(master, d_master, sizeof master, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(m, d_m, sizeof m, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(v, d_v, sizeof v, cudaMemcpyDeviceToHost));
+    for (int t = FIRST; t <= LAST; ++t) {
+        oracle_grad_norm(grads_k[t - FIRST], N, hyper.clip, &sumsq, &norm_o, &scale_o);
+        if (!(fabs((double)scale_o - (double)scales[t - FIRST]) <= 1e-6 * (double)scale_o)) {
+            fprintf(stderr, "step %d: scale %.9g vs oracle %.9g\n", t, scales[t - FIRST], scale_o);
+            return 1;
+        }
+        if (oracle_adamw_step(params_o, grads_k[t - FIRST], master_o, m_o, v_o, 0, N, otable, NT, hyper.lr,
+                              hyper.beta1, hyper.beta2, hyper.eps, hyper.weight_decay, scales[t - FIRST], t,
+                              10u + (uint32_t)t) != 0)
+            return 1;
+    }
+    float bc1_o, bc2_o;
+    oracle_bias_corrections(hyper.beta1, hyper.beta2, LAST, &bc1_o, &bc2_o);
+    if (status != 0 || state.t != LAST || state.seed != 10u + LAST || state.bc1 != bc1_o || state.bc2 != bc2_o) {
+        fprintf(stderr, "device step state t=%d seed=%u bc=(%.9g, %.9g), status %d\n", state.t, state.seed,
+                state.bc1, state.bc2, status);
+        ok = 0;
+    }
+    ok &= same(params, params_o, sizeof params, "params after graph steps");
+    ok &= same(master, master_o, sizeof master, "master after graph steps");
+    ok &= same(m, m_o, sizeof m, "m after graph steps");
+    ok &= same(v, v_o, sizeof v, "v after graph steps");
+    printf("c_abi_check: %s (n=%u, norm %.7g, scale %.7g; graph steps %d-%d)\n",
+           ok ? "bit-identical to the oracle" : "MISMATCH", N, norm1, scale1, FIRST, LAST);
+    cudaGraphExecDestroy(exec); cudaGraphDestroy(graph); cudaStreamDestroy(stream); free(bias);
+    cudaFree(d_bias); cudaFree(d_state);
     cudaFree(d_params); cudaFree(d_grads); cudaFree(d_sr); cudaFree(d_master); cudaFree(d_m); cudaFree(d_v);
     cudaFree(d_norm); cudaFree(d_scale); cudaFree(d_status); cudaFree(d_ws);
     return ok ? 0 : 1;
