@@ -56,9 +56,11 @@ SR_BYTES = 6
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only)
 STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
+                       "mixed_precision_adamw_gb300/csrc/mp_step.cuh",
                        "mixed_precision_adamw_gb300/csrc/mp_device.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
 SAMPLE_EVERY = 8
+GRAPH_STEPS = 20
 
 
 # ---------------------------------------------------------------------------
@@ -359,29 +361,48 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     out["stochastic_round"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
                                "gbs": round(SR_BYTES * N / ms / 1e6, 1),
                                "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
-    # The whole step as one captured CUDA graph (mp_optimizer_step_graph: the
-    # step count lives on the device), replayed once per step.
+    # Steps as CUDA graphs. "graph_step": one graph holding GRAPH_STEPS
+    # consecutive mp_optimizer_step_graph calls (the step count lives on the
+    # device, so each captured call is the next step), replayed back to back:
+    # the device time per step without per-launch host work.
+    # "graph_separate_kernels": the same with the separate calls (norm,
+    # finalize and update kernels: the general path) captured instead.
     opt.init_device_clock(t=1000, seed_base=W.BASE_SEED)
     opt.step_graph(st["params"], g, st["master"], st["m"], st["v"], stream=stream)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        opt.step_graph(st["params"], g, st["master"], st["m"], st["v"])
-    reps = max(iters, 200 if N < (1 << 24) else iters)
-    graph.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
+
+    def graph_ms(one_step):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(GRAPH_STEPS):
+                one_step()
+        reps = max(2, min(50, int(2e9 / max(1, 30 * N * GRAPH_STEPS))))
         graph.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        del graph
+        return a.elapsed_time(b) / (reps * GRAPH_STEPS), reps
+
+    ms, reps = graph_ms(lambda: opt.step_graph(st["params"], g, st["master"], st["m"], st["v"]))
     opt.check_status()
     out["graph_step"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
-                         "gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N / ms / 1e6, 1), "replays": reps,
-                         "what": "norm + AdamW + SR as one CUDA graph, replayed back to back (one event pair)"}
-    del graph
+                         "gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N / ms / 1e6, 1),
+                         "steps_per_graph": GRAPH_STEPS, "replays": reps,
+                         "what": "mp_optimizer_step_graph captured in a CUDA graph, replayed back to back"}
+
+    def separate():
+        mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N)
+        mp.mp_adamw_step(st["params"], g, st["master"], st["m"], st["v"], opt.table, d_grad_scale=opt.d_scale,
+                         t=7, seed=7, n=N, **kw)
+    ms, reps = graph_ms(separate)
+    out["graph_separate_kernels"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
+                                     "steps_per_graph": GRAPH_STEPS, "replays": reps,
+                                     "what": "mp_grad_norm + mp_adamw_step (3 kernels) captured the same way"}
     per = N // 8
 
     def shards():

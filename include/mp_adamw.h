@@ -31,7 +31,8 @@
  *  - Pointers must be aligned to their element size (2 B for bf16, 4 B for
  *    fp32, 8 B for fp64) or the call returns MP_ERR_ALIGN. Buffers that are
  *    also 16-B aligned take the vectorised kernels; others take scalar
- *    kernels that compute bit-identical results more slowly.
+ *    kernels that compute bit-identical updates and roundings more slowly
+ *    (the gradient norm's two paths differ in rounding: see mp_grad_norm).
  *  - Input and output buffers of one call must not overlap (params, grads,
  *    master, m and v are distinct arrays), and every device pointer must
  *    belong to the current device (cudaSetDevice) of the calling thread.
@@ -101,9 +102,12 @@ int mp_last_cuda_error(void);
  * The kernel squares in fp32 (exact for |g| in [2^-63, 2^64)), sums each
  * thread's terms with compensation, and reduces across threads and blocks in
  * fp64 in a fixed order; a block whose fp32 partial is non-finite or below
- * 2^-60 recomputes its share in fp64. The result is bit-identical on every
- * run with the same n on the same GPU model; its relative error against an
- * fp64 sum is below 1e-6 for any finite input.
+ * 2^-60 recomputes its share in fp64. Gradients that are 16-B aligned are
+ * read as 8-element vectors whose squares are added pairwise in fp32;
+ * others element by element, so the two differ in rounding. The result is
+ * bit-identical on every run with the same n and the same alignment class
+ * on the same GPU model; its relative error against an fp64 sum is below
+ * 1e-6 for any finite input.
  *
  *   grads       bf16[n], device, read only.
  *   n           element count; 0 gives sumsq 0, norm 0, scale 1.

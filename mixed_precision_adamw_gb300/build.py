@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmpadamw.so")
 
-SOURCES = ["mp_api.cu", "mp_step.cu", "mp_norm.cu", "mp_sr.cu", "mp_outlier.cu"]
+SOURCES = ["mp_api.cu", "mp_step.cu", "mp_norm.cu", "mp_sr.cu", "mp_outlier.cu", "mp_small.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-lineinfo", *GENCODE,

@@ -288,11 +288,33 @@ int optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_grads
   const int nb = mpk::norm_blocks(n, vec, dev);
   if (workspace_bytes < sizeof(double) * static_cast<size_t>(nb)) return MP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = mpk::launch_norm(src, n, vec, static_cast<double*>(workspace), nb, hyper->clip, d_norm, d_scale, nullptr,
-                       s, copy ? grads : nullptr, clock);
-  if (e == cudaSuccess && outlier_state != nullptr)
-    e = mpk::launch_outlier_check(outlier_state, d_norm, outlier_z, d_scale, d_z, d_status, s);
-  if (e == cudaSuccess && n != 0) e = launch_step(plan, params, grads, master, m, v, dev, s);
+  // The cluster kernel reads the update's gradients where the norm reads
+  // them (src), with 8-B vector loads like the update kernel's.
+  const bool small = n != 0 && n <= mpk::kSmallMaxN && plan.vec && aligned(src, 8) &&
+                     plan.seg_end.size() <= mpk::kSegCapSmall && nb <= mpk::kSmallClusterCtas &&
+                     mpk::small_step_available(dev, master != nullptr);
+  if (small) {  // one cluster launch, the same results as the three launches below
+    mpk::StepArgs a = plan.base;
+    a.params = params;
+    a.grads = grads;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.n = n;
+    a.goff = 0;
+    a.nseg = static_cast<uint32_t>(plan.seg_end.size());
+    a.first_decay = static_cast<uint32_t>(plan.seg_flag[0]);
+    const mpk::SmallArgs sa{src, copy ? grads : nullptr, nb, vec ? 1 : 0, hyper->clip, d_norm, d_scale,
+                            clock != nullptr ? *clock : mpk::StepClock{nullptr, nullptr, 0, nullptr},
+                            outlier_state, outlier_z, d_z};
+    e = mpk::launch_small_step(a, sa, plan.seg_end.data(), s);
+  } else {
+    e = mpk::launch_norm(src, n, vec, static_cast<double*>(workspace), nb, hyper->clip, d_norm, d_scale,
+                         nullptr, s, copy ? grads : nullptr, clock);
+    if (e == cudaSuccess && outlier_state != nullptr)
+      e = mpk::launch_outlier_check(outlier_state, d_norm, outlier_z, d_scale, d_z, d_status, s);
+    if (e == cudaSuccess && n != 0) e = launch_step(plan, params, grads, master, m, v, dev, s);
+  }
   if (e == cudaSuccess && host_norm != nullptr)
     e = cudaMemcpyAsync(host_norm, d_norm, sizeof(float), cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e);

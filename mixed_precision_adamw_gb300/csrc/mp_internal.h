@@ -90,6 +90,37 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
                         double* d_sumsq, cudaStream_t stream, uint16_t* copy_out = nullptr,
                         const StepClock* clock = nullptr);
 
+// One-launch step for small parameter sets (mp_small.cu): a cluster of
+// kSmallClusterCtas CTAs runs the norm, the optional outlier check and the
+// update, with results identical to the separate kernels; each CTA takes at
+// most one tile and one norm block. Used by the whole-step calls when
+// n <= kSmallMaxN, the update takes the vector path, the range has at most
+// kSegCapSmall decay segments, the general path's norm grid has at most
+// kSmallClusterCtas blocks and the GPU runs clusters of that size.
+constexpr int kSmallClusterCtas = 16;
+constexpr uint64_t kSmallMaxN = static_cast<uint64_t>(kSmallClusterCtas) * 2048;
+
+// Whether the current device can launch the small step's cluster (queried
+// once per device and variant).
+bool small_step_available(const DeviceInfo& dev, bool master);
+
+struct SmallArgs {
+  const uint16_t* norm_src;  // gradients the norm reads (device-visible address)
+  uint16_t* copy_out;        // non-null: norm_src is host memory, copied here (== StepArgs::grads)
+  int32_t nb;                // norm blocks of the general path for this n
+  int32_t norm_vec;          // the general path's norm takes 16-B vectors
+  float clip;
+  float* d_norm;
+  float* d_scale;            // the same buffer as StepArgs::d_scale, written here
+  StepClock clock;           // state == nullptr: t, seed, lr come from StepArgs
+  void* outlier;             // nullptr: no outlier check
+  float outlier_z;
+  double* d_z;
+};
+
+cudaError_t launch_small_step(const StepArgs& a, const SmallArgs& s, const uint64_t* seg_end,
+                              cudaStream_t stream);
+
 // Outlier check of the grad norm (mp_outlier.cu): d_state holds the window.
 cudaError_t launch_outlier_check(void* d_state, const float* d_norm, float z_threshold, float* d_scale,
                                  double* d_z, int32_t* d_status, cudaStream_t stream);

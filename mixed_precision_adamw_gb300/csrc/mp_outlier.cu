@@ -6,57 +6,22 @@
 // above a threshold. Here the detector runs as a one-thread kernel between
 // mp_grad_norm and mp_adamw_step, reading the norm and writing the clip scale
 // in device memory, so the step needs no host round trip: a skipped step is
-// a NaN scale (the step kernel then writes nothing) plus a status code.
-//
-// z = (x - mean) / std over the 128 most recent finite norms (population
-// standard deviation; both sums in window-slot order, fp64, one rounding per
-// operation); NaN until 128 norms have been seen; the check happens before x
-// joins the window; a non-finite norm never joins it.
+// a NaN scale (the step kernel then writes nothing) plus a status code. The
+// check itself (mp_outlier.cuh) is shared with the one-launch small step.
 #include <cmath>
 
 #include "mp_adamw.h"
 #include "mp_device.cuh"
 #include "mp_internal.h"
+#include "mp_outlier.cuh"
 
 namespace mpk {
 namespace {
 
-constexpr int kWindow = 128;
-
-struct OutlierState {
-  double window[kWindow];
-  unsigned long long count;  // finite norms pushed so far
-};
-
 __global__ void outlier_check_kernel(OutlierState* st, const float* d_norm, float z_threshold, float* d_scale,
                                      double* d_z, int32_t* d_status) {
   pdl_enter();
-  const double x = static_cast<double>(*d_norm);
-  const unsigned long long count = st->count;
-  double z = __longlong_as_double(0x7FF8000000000000ll);  // NaN until the window is full
-  if (count >= kWindow) {
-    double sum = 0.0;
-#pragma unroll 1
-    for (int i = 0; i < kWindow; ++i) sum = __dadd_rn(sum, st->window[i]);
-    const double mean = __ddiv_rn(sum, static_cast<double>(kWindow));
-    double ss = 0.0;
-#pragma unroll 1
-    for (int i = 0; i < kWindow; ++i) {
-      const double d = __dsub_rn(st->window[i], mean);
-      ss = __dadd_rn(ss, __dmul_rn(d, d));
-    }
-    const double sd = __dsqrt_rn(__ddiv_rn(ss, static_cast<double>(kWindow)));
-    z = __ddiv_rn(__dsub_rn(x, mean), sd);
-  }
-  if (d_z != nullptr) *d_z = z;
-  if (z_threshold > 0.0f && z > static_cast<double>(z_threshold)) {
-    *d_scale = __int_as_float(0x7FC00000);
-    if (d_status != nullptr) atomicCAS(d_status, 0, MP_SKIPPED_OUTLIER);
-  }
-  if (isfinite(x)) {
-    st->window[count % kWindow] = x;
-    st->count = count + 1;
-  }
+  if (outlier_update(st, *d_norm, z_threshold, d_z, d_status)) *d_scale = __int_as_float(0x7FC00000);
 }
 
 }  // namespace
