@@ -61,6 +61,7 @@ STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
 SAMPLE_EVERY = 8
 GRAPH_STEPS = 20
+MAX_LAUNCH_ELEMS = 3 << 26  # the library's elements per step launch (kMaxLaunchElems)
 
 
 # ---------------------------------------------------------------------------
@@ -277,7 +278,9 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return None
-    launches_per_step = 3  # norm partials + norm finalize + one step launch (<= 1024 decay segments)
+    # norm partials + norm finalize + the step launches (one per
+    # MAX_LAUNCH_ELEMS elements; every parameter set here has <= 1024 segments)
+    launches_per_step = 2 + -(-N // MAX_LAUNCH_ELEMS)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,

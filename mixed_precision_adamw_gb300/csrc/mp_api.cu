@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "mp_adamw.h"
+#include "mp_device.cuh"
 #include "mp_internal.h"
 
 namespace {
@@ -177,27 +178,32 @@ int plan_step(uint16_t* params, const uint16_t* grads, float* master, float* m, 
   return MP_OK;
 }
 
-// One launch per chunk of at most kSegCapLarge segments; chunk starts stay
+// One launch per chunk of at most kMaxLaunchElems elements (near-equal
+// chunks of whole tiles) and at most kSegCapLarge segments; chunk starts stay
 // multiples of 4 elements from `lo` so vector alignment is preserved.
 cudaError_t launch_step(const StepPlan& plan, uint16_t* params, const uint16_t* grads, float* master, float* m,
                         float* v, const mpk::DeviceInfo& dev, cudaStream_t s) {
   const std::vector<uint64_t>& seg_end = plan.seg_end;
   const uint64_t lo = plan.lo, hi = plan.hi;
   const size_t ns = seg_end.size();
+  const uint64_t pieces = (hi - lo + mpk::kMaxLaunchElems - 1) / mpk::kMaxLaunchElems;
+  const uint64_t tile = static_cast<uint64_t>(mpk::kTile);
+  const uint64_t chunk = ((hi - lo + pieces - 1) / pieces + tile - 1) / tile * tile;
   uint64_t c0 = lo;
   size_t s0 = 0;
   while (c0 < hi) {
-    uint64_t c1 = hi;
-    size_t last = ns - 1;
+    uint64_t c1 = hi - c0 > chunk ? c0 + chunk : hi;
     if (ns - s0 > mpk::kSegCapLarge) {
-      // Cut at the start of segment s0 + CAP - 1, rounded down to a multiple
-      // of 4 from lo. Segments s0+1 .. s0+CAP-2 hold >= 1 element each, so the
-      // chunk keeps >= 1020 elements and at most CAP - 1 segments.
+      // Cut at the start of segment s0 + CAP - 1 at the latest, rounded down
+      // to a multiple of 4 from lo. Segments s0+1 .. s0+CAP-2 hold >= 1
+      // element each, so the chunk keeps >= 1020 elements and at most CAP - 1
+      // segments.
       const uint64_t cut = seg_end[s0 + mpk::kSegCapLarge - 2];
-      c1 = lo + ((cut - lo) & ~static_cast<uint64_t>(3));
-      last = s0;
-      while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
+      const uint64_t c1s = lo + ((cut - lo) & ~static_cast<uint64_t>(3));
+      if (c1s < c1) c1 = c1s;
     }
+    size_t last = s0;
+    while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
     mpk::StepArgs a = plan.base;
     const uint64_t d = c0 - lo;
     a.params = params + d;

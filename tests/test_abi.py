@@ -204,3 +204,13 @@ def test_bias_table_checks(mp):
     assert L.mp_bias_table(0.9, 0.95, 4, None) == mp.MP_ERR_NULL
     assert L.mp_bias_table(0.9, 0.95, 0, FAKE) == mp.MP_ERR_RANGE
     assert L.mp_bias_table(1.0, 0.95, 4, FAKE) == mp.MP_ERR_RANGE
+
+
+def test_bench_counts_step_launches_like_the_library():
+    """bench.py's gpu_launches claim uses the library's per-launch element
+    limit; both must name the same number."""
+    import bench
+    text = open(os.path.join(ROOT, "mixed_precision_adamw_gb300", "csrc", "mp_internal.h")).read()
+    m = re.search(r"kMaxLaunchElems = uint64_t\{(\d+)\} << (\d+);", text)
+    assert m, "kMaxLaunchElems not found"
+    assert bench.MAX_LAUNCH_ELEMS == int(m.group(1)) << int(m.group(2))

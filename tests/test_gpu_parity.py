@@ -335,6 +335,48 @@ def test_step_many_segments_split_into_launches():
     _compare(d, host, "5000 segments")
 
 
+def test_long_range_split_by_size_and_segments_equals_small_shards():
+    """A range longer than one step launch takes (about 201M elements) with
+    more than 1024 decay segments: the library cuts it both by size and by
+    segment count; the result equals 16 small shard calls (no cuts of
+    either kind) bit for bit, and sampled windows equal the oracle."""
+    n = (3 << 27) + 777  # 402,654,001: three size cuts, plus segment cuts
+    gen = torch.Generator().manual_seed(11)
+    tab = W.random_table(n, gen, 1, 200_000)
+    assert len(tab) > 3000
+    g_dev = torch.randn(n, generator=torch.Generator(device="cuda").manual_seed(1), device="cuda")
+    grads = (g_dev * 1e-2).to(torch.bfloat16)
+    master = torch.randn(n, generator=torch.Generator(device="cuda").manual_seed(2), device="cuda") * 0.05
+    del g_dev
+    st = dict(params=master.to(torch.bfloat16), master=master, m=torch.zeros_like(master), v=torch.zeros_like(master))
+    kw = dict(lr=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, d_grad_scale=None, t=3, seed=9)
+    ttab = mp.TensorTable(tab)
+    win = [(0, 4096), (201_000_000, 201_700_000), (n - 5000, n)]
+    host = {}
+    for a, b in win:
+        host[a] = dict(params=W.bf16_bits(st["params"][a:b].cpu()).copy(), master=st["master"][a:b].cpu().numpy(),
+                       m=st["m"][a:b].cpu().numpy(), v=st["v"][a:b].cpu().numpy(),
+                       grads=W.bf16_bits(grads[a:b].cpu()).copy())
+    shards = {k: x.clone() for k, x in st.items()}
+    mp.mp_adamw_step(st["params"], grads, st["master"], st["m"], st["v"], ttab, **kw)
+    per = (n // 16) // 4 * 4
+    for r in range(16):
+        a = r * per
+        b = n if r == 15 else a + per
+        mp.mp_adamw_step(shards["params"][a:b], grads[a:b], shards["master"][a:b], shards["m"][a:b],
+                         shards["v"][a:b], ttab, global_offset=a, n=b - a, **kw)
+    torch.cuda.synchronize()
+    for k in st:
+        assert torch.equal(st[k].view(torch.int16) if k == "params" else st[k].view(torch.int32),
+                           shards[k].view(torch.int16) if k == "params" else shards[k].view(torch.int32)), k
+    del shards
+    for a, b in win:
+        h = host[a]
+        assert oracle.adamw_step(h["params"], h["grads"], h["master"], h["m"], h["v"], a, tab, 1e-2, 0.9, 0.95,
+                                 1e-8, 0.1, 1.0, 3, 9) == 0
+        _compare({k: st[k][a:b] for k in st}, h, f"window {a}")
+
+
 def test_shard_launches_equal_whole_buffer_and_oracle_windows():
     """GPT-2 1.5B shapes (1,557,686,400 params): the whole-buffer step and 8
     contiguous shard launches (the ZeRO-1 layout, no communication) are
