@@ -92,6 +92,21 @@ __device__ __forceinline__ uint32_t sr_bf16_c(float x, uint32_t draw_complement)
   return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : r;
 }
 
+// The same rounding, left in the high half of a 32-bit word (the low half is
+// left over): SR(x) = sr_bf16_hi(x, c) >> 16. Two such words pack into one
+// word of two bf16 with a single byte permute (pack_hi16), so the vector
+// paths spend no shifts on the results.
+__device__ __forceinline__ uint32_t sr_bf16_hi(float x, uint32_t draw_complement) {
+  const uint32_t b = __float_as_uint(x);
+  return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC00000u : b + draw_complement;
+}
+
+// (hi16(lo_word)) | (hi16(hi_word) << 16): bytes 2, 3 of lo_word, then bytes
+// 2, 3 of hi_word.
+__device__ __forceinline__ uint32_t pack_hi16(uint32_t lo_word, uint32_t hi_word) {
+  return __byte_perm(lo_word, hi_word, 0x7632);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }

@@ -29,10 +29,10 @@ sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t
     noise_pos4(goff + e0, pa);
     noise_pos4(goff + e1, pb);
     uint2 qa, qb;
-    qa.x = sr_bf16_c(a.x, draw16_complement(pa[0], seed)) | (sr_bf16_c(a.y, draw16_complement(pa[1], seed)) << 16);
-    qa.y = sr_bf16_c(a.z, draw16_complement(pa[2], seed)) | (sr_bf16_c(a.w, draw16_complement(pa[3], seed)) << 16);
-    qb.x = sr_bf16_c(b.x, draw16_complement(pb[0], seed)) | (sr_bf16_c(b.y, draw16_complement(pb[1], seed)) << 16);
-    qb.y = sr_bf16_c(b.z, draw16_complement(pb[2], seed)) | (sr_bf16_c(b.w, draw16_complement(pb[3], seed)) << 16);
+    qa.x = pack_hi16(sr_bf16_hi(a.x, draw16_complement(pa[0], seed)), sr_bf16_hi(a.y, draw16_complement(pa[1], seed)));
+    qa.y = pack_hi16(sr_bf16_hi(a.z, draw16_complement(pa[2], seed)), sr_bf16_hi(a.w, draw16_complement(pa[3], seed)));
+    qb.x = pack_hi16(sr_bf16_hi(b.x, draw16_complement(pb[0], seed)), sr_bf16_hi(b.y, draw16_complement(pb[1], seed)));
+    qb.y = pack_hi16(sr_bf16_hi(b.z, draw16_complement(pb[2], seed)), sr_bf16_hi(b.w, draw16_complement(pb[3], seed)));
     __stcs(reinterpret_cast<uint2*>(out + e0), qa);
     __stcs(reinterpret_cast<uint2*>(out + e1), qb);
   }

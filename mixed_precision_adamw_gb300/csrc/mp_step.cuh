@@ -96,11 +96,11 @@ __device__ __forceinline__ uint2 group_update(uint2 graw, float4& m4, float4& v4
 #pragma unroll
   for (int j = 0; j < kGroup; ++j) {
     w[j] = adamw_update(g[j], mm[j], vv[j], w[j], wd[j], scale, h);
-    r[j] = sr_bf16_c(w[j], draw16_complement(pos[j], seed));
+    r[j] = sr_bf16_hi(w[j], draw16_complement(pos[j], seed));
   }
   m4 = make_float4(mm[0], mm[1], mm[2], mm[3]);
   v4 = make_float4(vv[0], vv[1], vv[2], vv[3]);
-  return make_uint2(r[0] | (r[1] << 16), r[2] | (r[3] << 16));
+  return make_uint2(pack_hi16(r[0], r[1]), pack_hi16(r[2], r[3]));
 }
 
 // One element's inputs: its gradient, m, v and old weight.
