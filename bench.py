@@ -61,7 +61,6 @@ STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
 SAMPLE_EVERY = 8
 GRAPH_STEPS = 20
-MAX_LAUNCH_ELEMS = 3 << 26  # the library's elements per step launch (kMaxLaunchElems)
 
 
 # ---------------------------------------------------------------------------
@@ -278,9 +277,8 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return None
-    # norm partials + norm finalize + the step launches (one per
-    # MAX_LAUNCH_ELEMS elements; every parameter set here has <= 1024 segments)
-    launches_per_step = 2 + -(-N // MAX_LAUNCH_ELEMS)
+    # norm partials + norm finalize + the step's launches, as the library splits them
+    launches_per_step = 2 + len(mp.mp_step_launches(0, N, opt.table))
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,

@@ -184,6 +184,32 @@ int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master,
                   void* stream);
 
 /* ---------------------------------------------------------------------------
+ * How mp_adamw_step splits a range into kernel launches (host only; no CUDA
+ * call). Each launch covers at most 201,326,592 elements (long ranges are
+ * cut into near-equal launches of whole 2048-element tiles: on GB300 one
+ * persistent launch over billions of elements streams about 1 % slower) and
+ * at most 1024 decay segments (the table a launch carries in its kernel
+ * parameters); launch offsets stay multiples of 4 elements from
+ * global_offset. The whole-step calls use the same split for their update,
+ * except that a small set (n <= 32,768) runs in one cluster launch.
+ *
+ *   global_offset, n, table, n_tensors   as mp_adamw_step.
+ *   out        host array of `capacity` entries, or NULL with capacity 0;
+ *              receives the first min(capacity, count) launches in order.
+ *   count      host int64[1]: the number of launches.
+ * Errors: MP_ERR_NULL, MP_ERR_RANGE, MP_ERR_TABLE.
+ * ------------------------------------------------------------------------- */
+typedef struct mp_launch {
+    uint64_t offset;      /* global index of the launch's first element */
+    uint64_t size;        /* elements in the launch */
+    uint32_t segments;    /* decay segments it carries */
+    uint32_t first_decay; /* decay flag of its first segment (flags alternate) */
+} mp_launch_t;
+
+int mp_step_launches(uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                     mp_launch_t* out, int64_t capacity, int64_t* count);
+
+/* ---------------------------------------------------------------------------
  * Stochastic rounding fp32 -> bf16 of a range — [LLMC] §2.3 (the rounding
  * rule) and §5.2 (rebuilding bf16 weights from the fp32 master with the
  * saved rounding randomness).

@@ -50,6 +50,12 @@ class MpHyper(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("clip", ctypes.c_float)]
 
 
+class MpLaunch(ctypes.Structure):
+    """mp_launch_t: one kernel launch of a step (mp_step_launches)."""
+    _fields_ = [("offset", ctypes.c_uint64), ("size", ctypes.c_uint64), ("segments", ctypes.c_uint32),
+                ("first_decay", ctypes.c_uint32)]
+
+
 class MpStepState(ctypes.Structure):
     """mp_step_state_t: the device step counter of replayable steps (32 B)."""
     _fields_ = [("t", ctypes.c_int32), ("seed_base", ctypes.c_uint32), ("lr", ctypes.c_float),
@@ -93,6 +99,9 @@ def _load():
                                     vp, vp, vp, vp, vp]
     L.mp_grad_norm_noalloc.restype = ctypes.c_int
     L.mp_grad_norm_noalloc.argtypes = [vp, u64, f32, vp, vp, vp, vp]
+    L.mp_step_launches.restype = ctypes.c_int
+    L.mp_step_launches.argtypes = [u64, u64, ctypes.POINTER(MpTensor), i32, vp, ctypes.c_int64,
+                                   ctypes.POINTER(ctypes.c_int64)]
     L.mp_bias_table_len.restype = ctypes.c_int64
     L.mp_bias_table_len.argtypes = [f32, f32]
     L.mp_bias_table.restype = ctypes.c_int
@@ -279,6 +288,18 @@ def mp_optimizer_step(params: torch.Tensor, grads: torch.Tensor, master: Optiona
     _check(st, "mp_optimizer_step")
 
 
+def mp_step_launches(global_offset: int, n: int, table: "TensorTable"):
+    """How mp_adamw_step splits [global_offset, global_offset + n) into kernel
+    launches: a list of (offset, size, segments, first_decay). Host only."""
+    count = ctypes.c_int64()
+    _check(_lib.mp_step_launches(global_offset, n, table.ctypes_array, table.n_tensors, None, 0,
+                                 ctypes.byref(count)), "mp_step_launches")
+    out = (MpLaunch * max(1, count.value))()
+    _check(_lib.mp_step_launches(global_offset, n, table.ctypes_array, table.n_tensors, out, count.value,
+                                 ctypes.byref(count)), "mp_step_launches")
+    return [(x.offset, x.size, x.segments, x.first_decay) for x in out[:count.value]]
+
+
 def mp_bias_table_len(beta1: float, beta2: float) -> int:
     """Entries the bias-correction table needs (0: betas out of range)."""
     return int(_lib.mp_bias_table_len(beta1, beta2))
@@ -455,5 +476,5 @@ __all__ = [
     "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
     "mp_stochastic_round", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
-    "MpStepState", "LIB_PATH",
+    "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH",
 ]

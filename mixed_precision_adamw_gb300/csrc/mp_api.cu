@@ -109,6 +109,80 @@ int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip, void* workspace,
 
 namespace {
 
+// Checks the range and the tensor table (sorted, contiguous from 0, flags in
+// {0, 1}, covering [global_offset, global_offset + n)) and lists the decay
+// segments over the range: maximal runs of equal flag, so flags alternate;
+// seg_end[s] is one past segment s. No CUDA call.
+int table_segments(uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                   std::vector<uint64_t>* seg_end, std::vector<int>* seg_flag) {
+  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
+  if (table == nullptr) return MP_ERR_NULL;
+  if (n_tensors < 1) return MP_ERR_TABLE;
+  uint64_t off = 0;
+  for (int32_t k = 0; k < n_tensors; ++k) {
+    const mp_tensor_t& T = table[k];
+    if (T.offset != off || T.size > kMaxN || (T.decay != 0 && T.decay != 1) || T.reserved != 0)
+      return MP_ERR_TABLE;
+    off += T.size;
+    if (off > kMaxN) return MP_ERR_TABLE;
+  }
+  const uint64_t lo = global_offset, hi = global_offset + n;
+  if (off < hi) return MP_ERR_TABLE;
+  seg_end->clear();
+  seg_flag->clear();
+  for (int32_t k = 0; k < n_tensors; ++k) {
+    const uint64_t a = table[k].offset, b = table[k].offset + table[k].size;
+    if (b <= lo || a >= hi || a == b) continue;
+    const uint64_t end = b < hi ? b : hi;
+    if (!seg_flag->empty() && seg_flag->back() == table[k].decay) {
+      seg_end->back() = end;
+    } else {
+      seg_end->push_back(end);
+      seg_flag->push_back(table[k].decay);
+    }
+  }
+  return MP_OK;
+}
+
+// One step launch: elements [c0, c1) and decay segments s0 .. last.
+struct Chunk {
+  uint64_t c0, c1;
+  size_t s0, last;
+};
+
+// How a step over [lo, hi) with these segments is split into launches: at
+// most kMaxLaunchElems elements (near-equal chunks of whole tiles) and at
+// most kSegCapLarge segments each; chunk starts stay multiples of 4
+// elements from lo so vector alignment is preserved.
+std::vector<Chunk> split_launches(uint64_t lo, uint64_t hi, const std::vector<uint64_t>& seg_end) {
+  std::vector<Chunk> out;
+  const size_t ns = seg_end.size();
+  if (hi <= lo || ns == 0) return out;
+  const uint64_t pieces = (hi - lo + mpk::kMaxLaunchElems - 1) / mpk::kMaxLaunchElems;
+  const uint64_t tile = static_cast<uint64_t>(mpk::kTile);
+  const uint64_t chunk = ((hi - lo + pieces - 1) / pieces + tile - 1) / tile * tile;
+  uint64_t c0 = lo;
+  size_t s0 = 0;
+  while (c0 < hi) {
+    uint64_t c1 = hi - c0 > chunk ? c0 + chunk : hi;
+    if (ns - s0 > mpk::kSegCapLarge) {
+      // Cut at the start of segment s0 + CAP - 1 at the latest, rounded down
+      // to a multiple of 4 from lo. Segments s0+1 .. s0+CAP-2 hold >= 1
+      // element each, so the chunk keeps >= 1020 elements and at most CAP - 1
+      // segments.
+      const uint64_t cut = seg_end[s0 + mpk::kSegCapLarge - 2];
+      const uint64_t c1s = lo + ((cut - lo) & ~static_cast<uint64_t>(3));
+      if (c1s < c1) c1 = c1s;
+    }
+    size_t last = s0;
+    while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
+    out.push_back(Chunk{c0, c1, s0, last});
+    c0 = c1;
+    while (s0 < ns && seg_end[s0] <= c0) ++s0;
+  }
+  return out;
+}
+
 // A validated step: decay segments over [lo, hi) and the launch scalars.
 struct StepPlan {
   std::vector<uint64_t> seg_end;
@@ -132,36 +206,10 @@ int plan_step(uint16_t* params, const uint16_t* grads, float* master, float* m, 
   if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(weight_decay) || !(beta1 >= 0.0f) ||
       !(beta1 < 1.0f) || !(beta2 >= 0.0f) || !(beta2 < 1.0f) || t < 1)
     return MP_ERR_RANGE;
-  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
-  if (n_tensors < 1) return MP_ERR_TABLE;
-
-  // The table must tile [0, total) contiguously and cover the range.
-  uint64_t off = 0;
-  for (int32_t k = 0; k < n_tensors; ++k) {
-    const mp_tensor_t& T = table[k];
-    if (T.offset != off || T.size > kMaxN || (T.decay != 0 && T.decay != 1) || T.reserved != 0)
-      return MP_ERR_TABLE;
-    off += T.size;
-    if (off > kMaxN) return MP_ERR_TABLE;
-  }
+  const int st = table_segments(global_offset, n, table, n_tensors, &plan->seg_end, &plan->seg_flag);
+  if (st != MP_OK) return st;
   plan->lo = global_offset;
   plan->hi = global_offset + n;
-  if (off < plan->hi) return MP_ERR_TABLE;
-
-  // Decay segments over [lo, hi): maximal runs of equal flag, so flags alternate.
-  plan->seg_end.clear();
-  plan->seg_flag.clear();
-  for (int32_t k = 0; k < n_tensors; ++k) {
-    const uint64_t a = table[k].offset, b = table[k].offset + table[k].size;
-    if (b <= plan->lo || a >= plan->hi || a == b) continue;
-    const uint64_t end = b < plan->hi ? b : plan->hi;
-    if (!plan->seg_flag.empty() && plan->seg_flag.back() == table[k].decay) {
-      plan->seg_end.back() = end;
-    } else {
-      plan->seg_end.push_back(end);
-      plan->seg_flag.push_back(table[k].decay);
-    }
-  }
 
   mpk::StepArgs& base = plan->base;
   base.d_scale = d_grad_scale;
@@ -178,49 +226,26 @@ int plan_step(uint16_t* params, const uint16_t* grads, float* master, float* m, 
   return MP_OK;
 }
 
-// One launch per chunk of at most kMaxLaunchElems elements (near-equal
-// chunks of whole tiles) and at most kSegCapLarge segments; chunk starts stay
-// multiples of 4 elements from `lo` so vector alignment is preserved.
+// One launch per chunk of split_launches.
 cudaError_t launch_step(const StepPlan& plan, uint16_t* params, const uint16_t* grads, float* master, float* m,
                         float* v, const mpk::DeviceInfo& dev, cudaStream_t s) {
   const std::vector<uint64_t>& seg_end = plan.seg_end;
-  const uint64_t lo = plan.lo, hi = plan.hi;
-  const size_t ns = seg_end.size();
-  const uint64_t pieces = (hi - lo + mpk::kMaxLaunchElems - 1) / mpk::kMaxLaunchElems;
-  const uint64_t tile = static_cast<uint64_t>(mpk::kTile);
-  const uint64_t chunk = ((hi - lo + pieces - 1) / pieces + tile - 1) / tile * tile;
-  uint64_t c0 = lo;
-  size_t s0 = 0;
-  while (c0 < hi) {
-    uint64_t c1 = hi - c0 > chunk ? c0 + chunk : hi;
-    if (ns - s0 > mpk::kSegCapLarge) {
-      // Cut at the start of segment s0 + CAP - 1 at the latest, rounded down
-      // to a multiple of 4 from lo. Segments s0+1 .. s0+CAP-2 hold >= 1
-      // element each, so the chunk keeps >= 1020 elements and at most CAP - 1
-      // segments.
-      const uint64_t cut = seg_end[s0 + mpk::kSegCapLarge - 2];
-      const uint64_t c1s = lo + ((cut - lo) & ~static_cast<uint64_t>(3));
-      if (c1s < c1) c1 = c1s;
-    }
-    size_t last = s0;
-    while (seg_end[last] < c1) ++last;  // the segment holding element c1 - 1
+  for (const Chunk& c : split_launches(plan.lo, plan.hi, seg_end)) {
     mpk::StepArgs a = plan.base;
-    const uint64_t d = c0 - lo;
+    const uint64_t d = c.c0 - plan.lo;
     a.params = params + d;
     a.grads = grads + d;
     a.master = master ? master + d : nullptr;
     a.m = m + d;
     a.v = v + d;
-    a.n = c1 - c0;
-    a.goff = c0;
-    a.nseg = static_cast<uint32_t>(last - s0 + 1);
-    a.first_decay = static_cast<uint32_t>(plan.seg_flag[s0]);
-    std::vector<uint64_t> ends(seg_end.begin() + s0, seg_end.begin() + last + 1);
-    ends.back() = c1;
+    a.n = c.c1 - c.c0;
+    a.goff = c.c0;
+    a.nseg = static_cast<uint32_t>(c.last - c.s0 + 1);
+    a.first_decay = static_cast<uint32_t>(plan.seg_flag[c.s0]);
+    std::vector<uint64_t> ends(seg_end.begin() + c.s0, seg_end.begin() + c.last + 1);
+    ends.back() = c.c1;
     const cudaError_t e = mpk::launch_adamw(a, ends.data(), plan.vec, dev, s);
     if (e != cudaSuccess) return e;
-    c0 = c1;
-    while (s0 < ns && seg_end[s0] <= c0) ++s0;
   }
   return cudaSuccess;
 }
@@ -371,6 +396,25 @@ int mp_optimizer_step_graph(uint16_t* params, uint16_t* grads, const uint16_t* h
   return optimizer_step(params, grads, host_grads, master, m, v, n, table, n_tensors, hyper, 1, 0, &clock,
                         workspace, workspace_bytes, outlier_state, outlier_z, d_z, d_norm, d_scale, d_status,
                         host_norm, stream);
+}
+
+int mp_step_launches(uint64_t global_offset, uint64_t n, const mp_tensor_t* table, int32_t n_tensors,
+                     mp_launch_t* out, int64_t capacity, int64_t* count) {
+  if (count == nullptr || (capacity > 0 && out == nullptr)) return MP_ERR_NULL;
+  if (capacity < 0) return MP_ERR_RANGE;
+  std::vector<uint64_t> seg_end;
+  std::vector<int> seg_flag;
+  const int st = table_segments(global_offset, n, table, n_tensors, &seg_end, &seg_flag);
+  if (st != MP_OK) return st;
+  const std::vector<Chunk> chunks = split_launches(global_offset, global_offset + n, seg_end);
+  *count = static_cast<int64_t>(chunks.size());
+  for (size_t i = 0; i < chunks.size() && static_cast<int64_t>(i) < capacity; ++i) {
+    out[i].offset = chunks[i].c0;
+    out[i].size = chunks[i].c1 - chunks[i].c0;
+    out[i].segments = static_cast<uint32_t>(chunks[i].last - chunks[i].s0 + 1);
+    out[i].first_decay = static_cast<uint32_t>(seg_flag[chunks[i].s0]);
+  }
+  return MP_OK;
 }
 
 int mp_stochastic_round(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n, uint32_t seed,

@@ -206,11 +206,55 @@ def test_bias_table_checks(mp):
     assert L.mp_bias_table(1.0, 0.95, 4, FAKE) == mp.MP_ERR_RANGE
 
 
-def test_bench_counts_step_launches_like_the_library():
-    """bench.py's gpu_launches claim uses the library's per-launch element
-    limit; both must name the same number."""
-    import bench
-    text = open(os.path.join(ROOT, "mixed_precision_adamw_gb300", "csrc", "mp_internal.h")).read()
-    m = re.search(r"kMaxLaunchElems = uint64_t\{(\d+)\} << (\d+);", text)
-    assert m, "kMaxLaunchElems not found"
-    assert bench.MAX_LAUNCH_ELEMS == int(m.group(1)) << int(m.group(2))
+@pytest.mark.parametrize("seed,n,goff,tmax", [(1, 10, 0, 3), (2, 100_000, 0, 5000), (3, 100_003, 17, 40),
+                                           (4, 2_000_000, 5, 300), (5, (3 << 26) * 2 + 999, 0, 10 ** 7),
+                                           (6, (3 << 26) + 1, 3, 200_000)])
+def test_step_launch_plan_invariants(mp, seed, n, goff, tmax):
+    """mp_step_launches (the split mp_adamw_step launches with): launches tile
+    the range in order, each holds at most 201,326,592 elements and at most
+    1024 decay segments, starts stay 4-element aligned from the range start,
+    and the segment counts and first flags match the table."""
+    import torch
+    import workloads as W
+    gen = torch.Generator().manual_seed(seed)
+    tab = W.random_table(goff + n, gen, 1, tmax)
+    plan = mp.mp_step_launches(goff, n, mp.TensorTable(tab))
+    assert plan and plan[0][0] == goff and plan[-1][0] + plan[-1][1] == goff + n
+    for (o0, s0, _, _), (o1, _, _, _) in zip(plan, plan[1:]):
+        assert o0 + s0 == o1
+    # decay flag of every element boundary, from the table
+    starts = [o for o, _, _ in tab]
+    import bisect
+
+    def flag_at(i):
+        return tab[bisect.bisect_right(starts, i) - 1][2]
+
+    def segments(a, b):
+        cnt, prev, i = 0, None, a
+        k = bisect.bisect_right(starts, a) - 1
+        while i < b:
+            o, sz, d = tab[k]
+            if d != prev:
+                cnt, prev = cnt + 1, d
+            i = o + sz
+            k += 1
+        return cnt
+    for off, size, nseg, first in plan:
+        assert 1 <= size <= 3 << 26 and (off - goff) % 4 == 0
+        assert 1 <= nseg <= 1024 and first == flag_at(off)
+        assert nseg == segments(off, off + size)
+    if n <= 3 << 26 and segments(goff, goff + n) <= 1024:
+        assert len(plan) == 1
+
+
+def test_step_launch_plan_checks(mp):
+    L = mp.lib()
+    tab = mp.TensorTable([(0, 100, 1)])
+    import ctypes as C
+    cnt = C.c_int64()
+    assert L.mp_step_launches(0, 100, tab.ctypes_array, 1, None, 0, None) == mp.MP_ERR_NULL
+    assert L.mp_step_launches(0, 100, tab.ctypes_array, 1, None, 4, C.byref(cnt)) == mp.MP_ERR_NULL
+    assert L.mp_step_launches(0, 100, tab.ctypes_array, 1, None, -1, C.byref(cnt)) == mp.MP_ERR_RANGE
+    assert L.mp_step_launches(0, 101, tab.ctypes_array, 1, None, 0, C.byref(cnt)) == mp.MP_ERR_TABLE
+    assert L.mp_step_launches(0, 100, None, 1, None, 0, C.byref(cnt)) == mp.MP_ERR_NULL
+    assert L.mp_step_launches(0, 100, tab.ctypes_array, 1, None, 0, C.byref(cnt)) == mp.MP_OK and cnt.value == 1
