@@ -86,6 +86,57 @@ def test_whole_step_equals_separate_kernels(n, with_master):
             assert _same(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("n,nseg_max", [(20_000, 200), (32_768, 300)])
+def test_many_segments_take_the_general_path(n, nseg_max):
+    """More than 32 decay segments do not fit the cluster kernel's table: the
+    whole-step call then runs the general path, with the same results."""
+    tab, st, grads = _case(n, 7 * n, True, nseg_max=nseg_max)
+    assert _nseg(tab) > 32
+    a, b = _clone(st), _clone(st)
+    opt = mp.Optimizer(tab, clip=H["clip"], **KW)
+    ref = mp.Optimizer(tab, clip=H["clip"], **KW)
+    before = _sentinel(opt.workspace)
+    opt.step(a["params"], grads[0], a["master"], a["m"], a["v"], 1, 3)
+    mp.mp_grad_norm(grads[0], H["clip"], ref.workspace, ref.d_norm, ref.d_scale)
+    mp.mp_adamw_step(b["params"], grads[0], b["master"], b["m"], b["v"], ref.table, d_grad_scale=ref.d_scale,
+                     t=1, seed=3, **KW)
+    torch.cuda.synchronize()
+    assert not torch.equal(opt.workspace, before)
+    for k in a:
+        assert _same(a[k], b[k]), k
+
+
+def test_small_step_graph_with_host_gradients():
+    """The tiny set as a captured graph reading pinned host gradients: the
+    cluster kernel in a graph, against ordinary whole-step calls."""
+    name = "tiny"
+    tab = W.table(W.layout(W.specs_for(name)))
+    st = {k: x.cuda() for k, x in W.make_state(name).items()}
+    n = st["m"].numel()
+    a, b = _clone(st), _clone(st)
+    grads = [W.make_grads(name, t) for t in range(1, 9)]
+    ref = mp.Optimizer(tab, clip=H["clip"], **KW)
+    for t, g in enumerate(grads, start=1):
+        ref.step(a["params"], g.cuda(), a["master"], a["m"], a["v"], t, 50 + t)
+    opt = mp.Optimizer(tab, clip=H["clip"], **KW)
+    opt.init_device_clock(t=0, seed_base=50)
+    host_g = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    dev_g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    host_g.copy_(grads[0])
+    opt.step_graph(b["params"], dev_g, b["master"], b["m"], b["v"], host_grads=host_g)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        opt.step_graph(b["params"], dev_g, b["master"], b["m"], b["v"], host_grads=host_g)
+    for g in grads[1:]:
+        host_g.copy_(g)
+        graph.replay()
+        torch.cuda.synchronize()
+    assert opt.take_status() == 0 and opt.device_clock()["t"] == len(grads)
+    for k in a:
+        assert _same(a[k], b[k]), k
+
+
 def test_tiny_set_takes_the_cluster_kernel():
     tab = W.table(W.layout(W.specs_for("tiny")))
     st = {k: x.cuda() for k, x in W.make_state("tiny").items()}
