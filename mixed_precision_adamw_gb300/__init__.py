@@ -384,9 +384,16 @@ class Optimizer:
 
     step() makes one mp_optimizer_step call on the given (default: current)
     stream — norm and clip scale, the optional outlier check, the AdamW + SR
-    update — and does not synchronise. take_status() (which synchronises)
+    update — and does not synchronise (up to 32,768 parameters the library
+    runs it as one cluster launch, otherwise as the norm, finalize and update
+    kernels; the results are the same). take_status() (which synchronises)
     tells whether a step was refused for a non-finite norm or skipped as an
     outlier; check_status() raises MpError instead.
+
+    For CUDA graphs, init_device_clock() moves the step count, rounding seed
+    and learning rate into device memory and step_graph() takes the next step
+    from there (mp_optimizer_step_graph): capture one step_graph() call and
+    replay the graph once per training step.
     """
 
     def __init__(self, table_entries: Sequence[Tuple[int, int, int]], *, lr: float, beta1: float,
