@@ -281,7 +281,12 @@ int mp_outlier_check(void* d_state, const float* d_norm, float z_threshold,
  * the whole buffer [0, n). Enqueues mp_grad_norm's kernels, mp_outlier_check
  * (if outlier_state != NULL) and mp_adamw_step's kernel(s); same arguments,
  * same results as making those calls in that order with global_offset 0.
- * (A ZeRO-1 shard calls the pieces: its norm must cover every shard.)
+ * A small set (n <= 32,768, buffers vector-aligned, at most 32 decay
+ * segments) runs as one thread-block cluster launch instead, with the same
+ * results and the workspace left untouched. The first call on a device asks
+ * the GPU whether it can run that cluster: make it before any stream
+ * capture. (A ZeRO-1 shard calls the pieces: its norm must cover every
+ * shard.)
  *
  *   grads        bf16[n], device. If host_grads is NULL, the gradients to use;
  *                otherwise it receives the device copy of host_grads.
