@@ -89,7 +89,7 @@ __device__ __forceinline__ void noise_pos4(uint64_t k0, uint32_t (&pos)[4]) {
 __device__ __forceinline__ uint32_t sr_bf16_c(float x, uint32_t draw_complement) {
   const uint32_t b = __float_as_uint(x);
   const uint32_t r = (b + draw_complement) >> 16;
-  return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : r;
+  return (x != x) ? 0x7FC0u : r;  // x != x: NaN (a float compare keeps the integer pipe free)
 }
 
 // The same rounding, left in the high half of a 32-bit word (the low half is
@@ -98,7 +98,7 @@ __device__ __forceinline__ uint32_t sr_bf16_c(float x, uint32_t draw_complement)
 // paths spend no shifts on the results.
 __device__ __forceinline__ uint32_t sr_bf16_hi(float x, uint32_t draw_complement) {
   const uint32_t b = __float_as_uint(x);
-  return ((b & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC00000u : b + draw_complement;
+  return (x != x) ? 0x7FC00000u : b + draw_complement;
 }
 
 // (hi16(lo_word)) | (hi16(hi_word) << 16): bytes 2, 3 of lo_word, then bytes
