@@ -53,6 +53,7 @@ STEP_BYTES_MASTER = 28   # 2 grad + 3x4 (master, m, v) read; 3x4 + 2 (param) wri
 STEP_BYTES_NOMASTER = 22
 NORM_BYTES = 2
 SR_BYTES = 6
+ACC_BYTES = 8  # accumulate: read bf16 + fp32, write bf16
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only)
 STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
@@ -362,6 +363,12 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     out["stochastic_round"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
                                "gbs": round(SR_BYTES * N / ms / 1e6, 1),
                                "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
+    # bf16 accumulation with stochastic rounding (params += master, in place)
+    ms = time_events(lambda: mp.mp_accumulate_sr(st["params"], st["master"], 9, n=N, stream=stream), iters,
+                     stream)
+    out["accumulate_sr"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
+                            "gbs": round(ACC_BYTES * N / ms / 1e6, 1),
+                            "frac": round(ACC_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": ACC_BYTES}
     # Steps as CUDA graphs. "graph_step": one graph holding GRAPH_STEPS
     # consecutive mp_optimizer_step_graph calls (the step count lives on the
     # device, so each captured call is the next step), replayed back to back:

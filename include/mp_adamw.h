@@ -224,6 +224,24 @@ int mp_stochastic_round(uint16_t* out, const float* in,
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Accumulation into bf16 with stochastic rounding — [LLMC] §2.3: the same
+ * rounding also writes the encoder's embedding gradients in the backward
+ * pass (dwte, dwpe): the stored bf16 value is widened to fp32, the fp32
+ * contribution added (one round-to-nearest addition) and the sum written
+ * back by stochastic rounding, so contributions far below a bf16 step are
+ * kept in expectation.
+ *
+ *   acc[i] = SR((float)acc[i] + delta[i], global_offset + i, seed)  for i < n
+ *
+ *   acc     bf16[n], device, read and written in place.
+ *   delta   fp32[n], device, read only; must not overlap acc.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_accumulate_sr(uint16_t* acc, const float* delta,
+                     uint64_t global_offset, uint64_t n, uint32_t seed,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * The rounding randomness itself — [LLMC] §2.3 and §7 name SquirrelNoise5 /
  * Get2dNoiseUint. noise(k, seed) is the 2D form of SquirrelNoise5 (Squirrel
  * Eiserloh's published counter-based noise hash) at x = low 32 bits of k,

@@ -432,6 +432,21 @@ int mp_stochastic_round(uint16_t* out, const float* in, uint64_t global_offset, 
   return MP_OK;
 }
 
+int mp_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_offset, uint64_t n, uint32_t seed,
+                     void* stream) {
+  if (n == 0) return MP_OK;
+  if (acc == nullptr || delta == nullptr) return MP_ERR_NULL;
+  if (!aligned(acc, 2) || !aligned(delta, 4)) return MP_ERR_ALIGN;
+  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(delta, 16) && aligned(acc, 8);
+  e = mpk::launch_accumulate_sr(acc, delta, global_offset, n, seed, vec, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
 int mp_noise_u32(uint32_t* out, uint64_t first_index, uint64_t n, uint32_t seed, void* stream) {
   if (n == 0) return MP_OK;
   if (out == nullptr) return MP_ERR_NULL;

@@ -1,11 +1,13 @@
-// mp_sr.cu — standalone stochastic rounding fp32 -> bf16 and the rounding
-// randomness itself.
+// mp_sr.cu — standalone stochastic rounding fp32 -> bf16, accumulation into
+// bf16 with stochastic rounding, and the rounding randomness itself.
 //
 // llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §2.3 (the rule)
 // and §5.2 (bf16 weights are rebuilt from the fp32 master with the saved
 // rounding randomness, so a resumed run is bit-identical). Because the draw is
 // keyed on the global element index, the rebuild needs no launch-geometry
-// alignment: any grid gives the same bits. HBM-bound: 6 B per element.
+// alignment: any grid gives the same bits. HBM-bound: 6 B per element. The
+// same section has the rounding write the encoder's embedding gradients: a
+// bf16 gradient plus an fp32 contribution, rounded back (8 B per element).
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -49,6 +51,51 @@ sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint6
     out[i] = static_cast<uint16_t>(sr_bf16_c(in[i], draw16_complement(noise_pos(goff + i), seed)));
 }
 
+// acc[i] = SR((float)acc[i] + delta[i], goff + i, seed), in place. Vector
+// path: acc 8-B aligned, delta 16-B aligned; the step's tiling.
+__global__ void __launch_bounds__(kThreads)
+accumulate_vec_kernel(uint16_t* __restrict__ acc, const float* __restrict__ delta, uint64_t goff, uint64_t n,
+                      uint32_t seed) {
+  pdl_enter();
+  const uint64_t ntiles = n / kTile;
+  for (uint64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const uint64_t e0 = tile * kTile + threadIdx.x * kGroup;
+    const uint64_t e1 = e0 + kThreads * kGroup;
+    const uint2 a0 = __ldcs(reinterpret_cast<const uint2*>(acc + e0));
+    const uint2 a1 = __ldcs(reinterpret_cast<const uint2*>(acc + e1));
+    const float4 d0 = __ldcs(reinterpret_cast<const float4*>(delta + e0));
+    const float4 d1 = __ldcs(reinterpret_cast<const float4*>(delta + e1));
+    uint32_t p0[kGroup], p1[kGroup];
+    noise_pos4(goff + e0, p0);
+    noise_pos4(goff + e1, p1);
+    uint2 q0, q1;
+    q0.x = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a0.x), d0.x), draw16_complement(p0[0], seed)),
+                     sr_bf16_hi(__fadd_rn(bf16_hi(a0.x), d0.y), draw16_complement(p0[1], seed)));
+    q0.y = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a0.y), d0.z), draw16_complement(p0[2], seed)),
+                     sr_bf16_hi(__fadd_rn(bf16_hi(a0.y), d0.w), draw16_complement(p0[3], seed)));
+    q1.x = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a1.x), d1.x), draw16_complement(p1[0], seed)),
+                     sr_bf16_hi(__fadd_rn(bf16_hi(a1.x), d1.y), draw16_complement(p1[1], seed)));
+    q1.y = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a1.y), d1.z), draw16_complement(p1[2], seed)),
+                     sr_bf16_hi(__fadd_rn(bf16_hi(a1.y), d1.w), draw16_complement(p1[3], seed)));
+    __stcs(reinterpret_cast<uint2*>(acc + e0), q0);
+    __stcs(reinterpret_cast<uint2*>(acc + e1), q1);
+  }
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = ntiles * kTile + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    acc[i] = static_cast<uint16_t>(
+        sr_bf16_c(__fadd_rn(bf16_to_f32(acc[i]), delta[i]), draw16_complement(noise_pos(goff + i), seed)));
+}
+
+__global__ void __launch_bounds__(kThreads)
+accumulate_scalar_kernel(uint16_t* __restrict__ acc, const float* __restrict__ delta, uint64_t goff, uint64_t n,
+                         uint32_t seed) {
+  pdl_enter();
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    acc[i] = static_cast<uint16_t>(
+        sr_bf16_c(__fadd_rn(bf16_to_f32(acc[i]), delta[i]), draw16_complement(noise_pos(goff + i), seed)));
+}
+
 __global__ void __launch_bounds__(kThreads)
 noise_kernel(uint32_t* __restrict__ out, uint64_t first, uint64_t n, uint32_t seed) {
   pdl_enter();
@@ -75,6 +122,16 @@ cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
     return launch_pdl(sr_vec_kernel, blocks, kThreads, stream, out, in, goff, n, seed);
   }
   return launch_pdl(sr_scalar_kernel, grid_for(n, dev), kThreads, stream, out, in, goff, n, seed);
+}
+
+cudaError_t launch_accumulate_sr(uint16_t* acc, const float* delta, uint64_t goff, uint64_t n, uint32_t seed,
+                                 bool vec, const DeviceInfo& dev, cudaStream_t stream) {
+  if (vec) {
+    const uint64_t ntiles = n / kTile;
+    const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);
+    return launch_pdl(accumulate_vec_kernel, blocks, kThreads, stream, acc, delta, goff, n, seed);
+  }
+  return launch_pdl(accumulate_scalar_kernel, grid_for(n, dev), kThreads, stream, acc, delta, goff, n, seed);
 }
 
 cudaError_t launch_noise(uint32_t* out, uint64_t first, uint64_t n, uint32_t seed, const DeviceInfo& dev,

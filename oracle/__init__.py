@@ -46,6 +46,8 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_stochastic_round.restype = None
     L.oracle_stochastic_round.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64,
                                           ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_accumulate_sr.restype = None
+    L.oracle_accumulate_sr.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
     L.oracle_sumsq.restype = ctypes.c_double
     L.oracle_sumsq.argtypes = [_c_u16p, ctypes.c_uint64]
     L.oracle_clip_scale.restype = ctypes.c_float
@@ -107,6 +109,14 @@ def stochastic_round(x: np.ndarray, global_offset: int, seed: int) -> np.ndarray
     lib().oracle_stochastic_round(_ptr(out, _c_u16p, np.uint16), _ptr(x, _c_f32p, np.float32),
                                   global_offset, x.size, seed)
     return out
+
+
+def accumulate_sr(acc: np.ndarray, delta: np.ndarray, global_offset: int, seed: int) -> None:
+    """In place: acc[i] = SR((float)acc[i] + delta[i], global_offset + i, seed)
+    (acc holds raw bf16 patterns as uint16)."""
+    assert acc.size == delta.size
+    lib().oracle_accumulate_sr(_ptr(acc, _c_u16p, np.uint16), _ptr(delta, _c_f32p, np.float32),
+                               global_offset, acc.size, seed)
 
 
 def sumsq(grads: np.ndarray) -> float:

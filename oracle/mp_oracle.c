@@ -95,6 +95,22 @@ void oracle_stochastic_round(uint16_t* out, const float* in,
         out[i] = oracle_sr(in[i], global_offset + i, seed);
 }
 
+/* ---- Accumulation with stochastic rounding -------------------------------
+ * [LLMC] §2.3: the same rounding also writes the embedding gradients of the
+ * encoder's backward pass (dwte, dwpe): the stored bf16 gradient is widened
+ * to fp32, the new fp32 contribution added, and the sum written back to bf16
+ * by stochastic rounding, so small contributions are kept in expectation
+ * instead of being rounded away. Keyed on (global index, seed) like every
+ * other draw here. */
+void oracle_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_offset, uint64_t n,
+                          uint32_t seed)
+{
+    for (uint64_t i = 0; i < n; ++i) {
+        const float sum = bf16_bits_to_float(acc[i]) + delta[i];
+        acc[i] = oracle_sr(sum, global_offset + i, seed);
+    }
+}
+
 /* ---- Gradient norm ---------------------------------------------------------
  * [LLMC] §4: the global norm of all gradients, then the clip scale
  * min(1, 1.0 / grad_norm). The threshold 1.0 is an argument here. */

@@ -47,6 +47,10 @@ uint16_t oracle_sr_with_rand(float x, uint32_t rand16);
 uint16_t oracle_sr(float x, uint64_t k, uint32_t seed);
 void oracle_stochastic_round(uint16_t* out, const float* in,
                              uint64_t global_offset, uint64_t n, uint32_t seed);
+/* acc[i] = SR((float)acc[i] + delta[i], global_offset + i, seed): a bf16
+ * accumulator updated in fp32 and rounded back stochastically. */
+void oracle_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_offset, uint64_t n,
+                          uint32_t seed);
 
 /* Gradient norm: plain fp64 sum of squares in index order, then sqrt. */
 double oracle_sumsq(const uint16_t* grads, uint64_t n);

@@ -74,7 +74,8 @@ def test_noise_bit_exact(first, seed, n):
 
 
 def _special_f32(n, rng):
-    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-45, 38, n)).astype(np.float32)
+    with np.errstate(over="ignore"):  # magnitudes past the fp32 range become +-Inf on purpose
+        x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-45, 38, n)).astype(np.float32)
     specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, np.finfo(np.float32).max,
                          -np.finfo(np.float32).max, 1e-45, -1e-45, 1.17549435e-38, 257.0, 1.0 + 2 ** -8],
                         np.float32)
@@ -100,6 +101,32 @@ def test_stochastic_round_bit_exact(n, pad_in, pad_out, goff):
     seed = 0xC0FFEE
     mp.mp_stochastic_round(out, xin, seed, global_offset=goff)
     assert_bit_equal(to_np_u16(out), oracle.stochastic_round(x, goff, seed), "sr")
+
+
+@pytest.mark.parametrize("n,pad_acc,pad_delta,goff", [
+    (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32), (1, 0, 0, 5),
+    (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000), (2048 * 7 + 5, 0, 0, (1 << 32) - 5001),
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), ((1 << 22) + 3, 0, 0, 123)])
+def test_accumulate_sr_bit_exact(n, pad_acc, pad_delta, goff):
+    """acc = SR((float)acc + delta): special values on both sides (NaN, Inf,
+    signed zeros, subnormals, the largest finite values), vector and scalar
+    paths, offsets across 2^32."""
+    rng = np.random.default_rng(n + 7 * pad_acc)
+    acc0 = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
+    acc0[:8] = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x7F7F, 0xFF7F, 0x0001], np.uint16)[: min(8, n)]
+    delta = _special_f32(n, rng) if n > 2000 else rng.standard_normal(n).astype(np.float32)
+    if n > 2000:
+        # ordinary magnitudes too: contributions around the accumulator's own scale
+        k = n // 2
+        with np.errstate(invalid="ignore", over="ignore"):  # NaN and Inf accumulators give NaN/Inf deltas
+            delta[k:] = (oracle.bf16_bits_to_f32(acc0[k:]) * rng.uniform(-1e-2, 1e-2, n - k)).astype(np.float32)
+    acc = dev_u16(acc0, pad_acc)
+    d = dev_f32(delta, pad_delta)
+    seed = 0xACC
+    mp.mp_accumulate_sr(acc, d, seed, global_offset=goff)
+    ref = acc0.copy()
+    oracle.accumulate_sr(ref, delta, goff, seed)
+    assert_bit_equal(to_np_u16(acc), ref, "accumulate_sr")
 
 
 def test_stochastic_round_full_size_and_drift():

@@ -70,6 +70,11 @@ MUTANTS = {
          "const double sd = sqrt(ss / (ORACLE_OUTLIER_WINDOW - 1));"),
     "outlier: z with the wrong sign":
         ("zz = (x - mean) / sd;", "zz = (mean - x) / sd;"),
+    "accumulate: contribution dropped":
+        ("const float sum = bf16_bits_to_float(acc[i]) + delta[i];",
+         "const float sum = bf16_bits_to_float(acc[i]);"),
+    "accumulate: draw keyed on the local index":
+        ("acc[i] = oracle_sr(sum, global_offset + i, seed);", "acc[i] = oracle_sr(sum, i, seed);"),
     "outlier: non-finite norms enter the window":
         ("    if (isfinite(x)) {\n        st->window", "    if (1) {\n        st->window"),
 }
@@ -104,6 +109,10 @@ def _pins():
         ("shards", lambda: P.test_sharded_steps_equal_whole_buffer_steps(True)),
         ("torch AdamW fp64", P.test_sixteen_steps_track_torch_adamw_fp64),
         ("sr tracks small updates", P.test_sr_tracks_small_updates_where_round_to_nearest_stalls),
+        ("accumulate zero", P.test_accumulate_sr_adding_zero_changes_nothing),
+        ("accumulate exact", P.test_accumulate_sr_exact_when_the_sum_is_representable),
+        ("accumulate unbiased", P.test_accumulate_sr_is_unbiased_over_seeds),
+        ("accumulate shards", P.test_accumulate_sr_keeps_small_contributions_and_shards),
     ]
 
 

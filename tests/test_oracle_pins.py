@@ -476,6 +476,84 @@ def test_sr_tracks_small_updates_where_round_to_nearest_stalls():
 
 
 # --------------------------------------------------------------------------
+# Accumulating into bf16 with stochastic rounding — llm.c ch. 04 §2.3: the
+# same rounding writes the encoder's embedding gradients (a bf16 gradient
+# plus an fp32 contribution, rounded back to bf16).
+# --------------------------------------------------------------------------
+def _bf16(vals):
+    return W.bf16_bits(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)).copy()
+
+
+def test_accumulate_sr_adding_zero_changes_nothing():
+    rng = np.random.default_rng(5)
+    acc = rng.integers(0, 1 << 16, 100_000, dtype=np.uint32).astype(np.uint16)
+    keep = (acc & 0x7F80) != 0x7F80  # drop NaN and Inf patterns
+    keep &= (acc & 0x7FFF) != 0      # and signed zeros (IEEE: -0 + +0 = +0)
+    acc = acc[keep]
+    out = acc.copy()
+    oracle.accumulate_sr(out, np.zeros(acc.size, np.float32), 123, 9)
+    assert np.array_equal(out, acc)
+    z = np.array([0x8000, 0x0000], np.uint16)  # -0 + 0 = +0, +0 + 0 = +0 (round to nearest)
+    oracle.accumulate_sr(z, np.zeros(2, np.float32), 0, 1)
+    assert z.tolist() == [0x0000, 0x0000]
+
+
+def test_accumulate_sr_exact_when_the_sum_is_representable():
+    # integers up to 256 are exact in bf16 ([CMU13] §7.3 ex. 5: 257 is not)
+    a = np.arange(0, 129, dtype=np.float32)
+    d = np.arange(0, 129, dtype=np.float32)[::-1].copy()  # a + d = 128
+    acc = _bf16(a)
+    oracle.accumulate_sr(acc, d, 0, 77)
+    assert np.array_equal(oracle.bf16_bits_to_f32(acc), np.full(a.size, 128.0, np.float32))
+    acc = _bf16([1.0, -2.0, 0.5])
+    # one bf16 step at each magnitude: 2^-7 at 1, 2^-6 at 2, 2^-8 at 0.5
+    oracle.accumulate_sr(acc, np.array([2.0 ** -7, -2.0 ** -6, 2.0 ** -8], np.float32), 0, 3)
+    assert np.array_equal(oracle.bf16_bits_to_f32(acc), np.array([1 + 2.0 ** -7, -2 - 2.0 ** -6, 0.5 + 2.0 ** -8],
+                                                                   np.float32))
+
+
+def test_accumulate_sr_is_unbiased_over_seeds():
+    """1 + 0.3 ulp: over 10^5 seeds the mean result is 1 + 0.3 ulp within 4σ."""
+    ulp = 2.0 ** -7
+    seeds = 100_000
+    res = np.empty(seeds, np.float32)
+    for s in range(seeds):
+        acc = np.array([0x3F80], np.uint16)
+        oracle.accumulate_sr(acc, np.array([0.3 * ulp], np.float32), 42, s)
+        res[s] = oracle.bf16_bits_to_f32(acc)[0]
+    x = float(np.float32(1.0) + np.float32(0.3 * ulp))
+    p = (x - 1.0) / ulp
+    assert set(np.unique(res).tolist()) <= {1.0, 1.0 + ulp}
+    sigma = ulp * math.sqrt(p * (1 - p) / seeds)
+    assert abs(float(res.astype(np.float64).mean()) - x) < 4 * sigma
+
+
+def test_accumulate_sr_keeps_small_contributions_and_shards():
+    """1000 contributions of 1e-4·|a0| each (below half a bf16 step): the
+    rounded accumulator follows the fp32 sum where round-to-nearest stalls;
+    accumulating the buffer as two shards at their global offsets gives the
+    same bits as the whole buffer."""
+    n = 1 << 14
+    a0 = W.sr_stress_weights(n, seed=7).numpy()
+    delta = (np.float32(1e-4) * np.abs(a0)).astype(np.float32)
+    fp32 = a0.copy()
+    acc = W.bf16_bits(torch.from_numpy(a0).to(torch.bfloat16)).copy()
+    halves = acc.copy()
+    for t in range(1, 1001):
+        fp32 = (fp32 + delta).astype(np.float32)
+        oracle.accumulate_sr(acc, delta, 0, W.step_seed(t))
+        h0, h1 = halves[: n // 2].copy(), halves[n // 2:].copy()
+        oracle.accumulate_sr(h0, delta[: n // 2].copy(), 0, W.step_seed(t))
+        oracle.accumulate_sr(h1, delta[n // 2:].copy(), n // 2, W.step_seed(t))
+        halves = np.concatenate([h0, h1])
+    assert np.array_equal(acc, halves)
+    rel = float(np.mean(oracle.bf16_bits_to_f32(acc).astype(np.float64) / fp32 - 1.0))
+    assert abs(rel) < 2e-3
+    rne = torch.from_numpy(a0).to(torch.bfloat16)
+    assert torch.equal((rne.float() + torch.from_numpy(delta)).to(torch.bfloat16), rne)  # RNE never moves
+
+
+# --------------------------------------------------------------------------
 # Bit-perfect resume — llm.c ch. 04 §5.2: bf16 weights are not checkpointed;
 # they are rebuilt from the fp32 master with the saved rounding randomness.
 # With draws keyed on the global index, the rebuild is SR(master, seed_t).
