@@ -20,6 +20,13 @@
  * with one rounding per written operation and an explicit fmaf() for each of
  * the two-FMA lerps; the gradient norm is a plain fp64 sum of squares.
  * Compiled with -ffp-contract=off and without fast-math.
+ *
+ * Parity unpinned: the exact 32-bit values of oracle_noise_u32. The pages
+ * name SquirrelNoise5 but print no test vector, so the hash's constants and
+ * shifts are pinned only by statistical tests (uniform, uncorrelated draws)
+ * that a different but equally good mixer would also pass. Every other
+ * function here is pinned by values or properties the pages or mathematics
+ * fix (tests/test_oracle_pins.py).
  */
 #ifndef MP_ORACLE_H
 #define MP_ORACLE_H
