@@ -1,4 +1,5 @@
-"""Compile the CPU oracle (mp_oracle.c) into oracle/_mp_oracle.so with gcc.
+"""Compile the CPU oracle (mp_oracle.c) into oracle/_mp_oracle.so with gcc,
+and its command-line front end (mp_oracle_cli.c) into oracle/_mp_oracle_cli.
 
 Test infrastructure: the oracle is built next to its source so that the
 tests, the smoke check and the benchmark's CPU baseline can load it. The
@@ -13,6 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "mp_oracle.c")
 HDR = os.path.join(HERE, "mp_oracle.h")
 LIB = os.path.join(HERE, "_mp_oracle.so")
+CLI_SRC = os.path.join(HERE, "mp_oracle_cli.c")
+CLI = os.path.join(HERE, "_mp_oracle_cli")
 
 CFLAGS = [
     "-O2", "-std=c11", "-fPIC", "-shared",
@@ -21,20 +24,29 @@ CFLAGS = [
 ]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(out, sources) -> bool:
+    if not os.path.exists(out):
         return True
-    lib_t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > lib_t for p in (SRC, HDR))
+    t = os.path.getmtime(out)
+    return any(os.path.getmtime(p) > t for p in sources)
+
+
+def is_stale() -> bool:
+    return _stale(LIB, (SRC, HDR)) or _stale(CLI, (SRC, HDR, CLI_SRC))
 
 
 def build(force: bool = False) -> str:
-    """Build the oracle library if missing or older than its sources."""
-    if force or is_stale():
+    """Build the oracle library (and its command-line front end) if missing
+    or older than their sources."""
+    if force or _stale(LIB, (SRC, HDR)):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
+        subprocess.run(["gcc", *CFLAGS, SRC, "-o", tmp, "-lm"], check=True)
         os.replace(tmp, LIB)
+    if force or _stale(CLI, (SRC, HDR, CLI_SRC)):
+        tmp = CLI + f".tmp{os.getpid()}"
+        flags = [f for f in CFLAGS if f not in ("-shared", "-fPIC")]
+        subprocess.run(["gcc", *flags, SRC, CLI_SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, CLI)
     return LIB
 
 
