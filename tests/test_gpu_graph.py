@@ -247,3 +247,24 @@ def test_device_refuses_steps_it_cannot_count():
     opt_e = _opt(tab, beta1=0.0, beta2=0.0)
     opt_e.step(ref["params"], dg, ref["master"], ref["m"], ref["v"], 1001, 1 + 1001)
     _assert_same(ref, st, "betas 0, t = 1001")
+
+
+def test_empty_step_still_counts():
+    """n = 0: nothing to update, but the step count advances (the train loop's
+    step moves on) and the norm of nothing is 0 with scale 1."""
+    import ctypes
+    tab = mp.TensorTable([])
+    opt = _opt([(0, 8, 1)])
+    opt.init_device_clock(t=4, seed_base=10)
+    hyper = mp.MpHyper(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    st = mp.lib().mp_optimizer_step_graph(None, None, None, None, None, None, 0, tab.ctypes_array, 0,
+                                          ctypes.byref(hyper), opt.d_state.data_ptr(), opt.d_bias.data_ptr(),
+                                          opt.d_bias.numel() // 2, opt.workspace.data_ptr(),
+                                          opt.workspace.numel(), None, 0.0, None, opt.d_norm.data_ptr(),
+                                          opt.d_scale.data_ptr(), opt.d_status.data_ptr(), None, None)
+    assert st == mp.MP_OK
+    torch.cuda.synchronize()
+    clock = opt.device_clock()
+    assert clock["t"] == 5 and clock["seed"] == 15
+    assert float(opt.d_norm.item()) == 0.0 and float(opt.d_scale.item()) == 1.0
+    assert opt.take_status() == 0
