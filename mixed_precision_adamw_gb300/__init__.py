@@ -423,6 +423,8 @@ class Optimizer:
         self.d_scale = torch.zeros(1, dtype=torch.float32, device=dev)
         self.d_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.outlier = OutlierDetector(outlier_z, device=dev) if outlier_z is not None else None
+        self.d_state = None  # device step state of replayable steps (init_device_clock)
+        self.d_bias = None
 
     def step(self, params, grads, master, m, v, t: int, seed: int, host_grads=None, host_norm=None, stream=None):
         """One native call (mp_optimizer_step). With host_grads (pinned CPU
@@ -447,20 +449,26 @@ class Optimizer:
                                dtype=torch.int32)
         dev = self.d_norm.device
         with torch.cuda.stream(stream) if stream is not None else _nullcontext():
-            if getattr(self, "d_state", None) is None:
+            if self.d_state is None:
                 self.d_state = torch.empty(8, dtype=torch.int32, device=dev)
                 self.d_bias = mp_bias_table(self.hyper["beta1"], self.hyper["beta2"]).to(dev)
             self.d_state.copy_(raw)
 
+    def _need_clock(self):
+        if self.d_state is None:
+            raise RuntimeError("call init_device_clock() before the replayable-step methods")
+
     def set_lr(self, lr: float, stream=None):
         """Stream-ordered write of the next steps' learning rate into the
         device step state (between replays of a captured step)."""
+        self._need_clock()
         with torch.cuda.stream(stream) if stream is not None else _nullcontext():
             self.d_state[2:3].view(torch.float32).fill_(float(lr))
 
     def device_clock(self) -> dict:
         """The device step state (synchronises): t, seed_base, lr, and the
         seed and bias corrections of the last step taken."""
+        self._need_clock()
         raw = self.d_state.cpu().numpy().tobytes()
         st = MpStepState.from_buffer_copy(raw)
         return dict(t=st.t, seed_base=st.seed_base, lr=st.lr, seed=st.seed, bc1=st.bc1, bc2=st.bc2)
@@ -468,6 +476,7 @@ class Optimizer:
     def step_graph(self, params, grads, master, m, v, host_grads=None, host_norm=None, stream=None):
         """One mp_optimizer_step_graph call: the next step of the device
         clock. Capturable: record it once in a CUDA graph and replay it."""
+        self._need_clock()
         mp_optimizer_step_graph(params, grads, master, m, v, self.table, self.hyper_struct, d_state=self.d_state,
                                 d_bias=self.d_bias, workspace=self.workspace, d_norm=self.d_norm,
                                 d_scale=self.d_scale, d_status=self.d_status,
