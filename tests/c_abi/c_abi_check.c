@@ -5,11 +5,11 @@
  *
  * One optimizer step (mp_optimizer_step, then a second call of the pieces:
  * mp_grad_norm + mp_adamw_step) on n = 100,003 elements split into 7 tensors
- * with alternating decay flags, then mp_stochastic_round. Then steps 3-6 as
- * replayable steps: step 3 a plain mp_optimizer_step_graph call, steps 4-6
- * replays of one CUDA graph captured from a stream, with fresh gradients
- * copied in between. Exit status 0 when every output is bit-identical to the
- * oracle's.
+ * with alternating decay flags, then mp_stochastic_round and mp_accumulate_sr.
+ * Then steps 3-6 as replayable steps: step 3 a plain mp_optimizer_step_graph
+ * call, steps 4-6 replays of one CUDA graph captured from a stream, with
+ * fresh gradients copied in between. Exit status 0 when every output is
+ * bit-identical to the oracle's.
  */
 #include <math.h>
 #include <stdint.h>
@@ -111,8 +111,9 @@ int main(void) {
                      hyper.eps, hyper.weight_decay, d_scale, 2, 12, d_status, NULL));
     float scale2;
     CK(cudaMemcpy(&scale2, d_scale, 4, cudaMemcpyDeviceToHost));
-    /* standalone rounding of the new master */
+    /* standalone rounding of the new master, then accumulating the master into it */
     MP(mp_stochastic_round(d_sr, d_master, 0, N, 99, NULL));
+    MP(mp_accumulate_sr(d_sr, d_master, 0, N, 98, NULL));
     int32_t status;
     CK(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(params, d_params, sizeof params, cudaMemcpyDeviceToHost));
@@ -135,12 +136,13 @@ int main(void) {
                           hyper.beta2, hyper.eps, hyper.weight_decay, scale2, 2, 12) != 0)
         return 1;
     oracle_stochastic_round(out_sr_o, master_o, 0, N, 99);
+    oracle_accumulate_sr(out_sr_o, master_o, 0, N, 98);
     int ok = status == 0;
     ok &= same(params, params_o, sizeof params, "params");
     ok &= same(master, master_o, sizeof master, "master");
     ok &= same(m, m_o, sizeof m, "m");
     ok &= same(v, v_o, sizeof v, "v");
-    ok &= same(out_sr, out_sr_o, sizeof out_sr, "stochastic round");
+    ok &= same(out_sr, out_sr_o, sizeof out_sr, "stochastic round + accumulate");
 
     /* steps 3..6 with the step count on the device: seed of step t = 10 + t */
     enum { FIRST = 3, LAST = 6 };
