@@ -43,6 +43,25 @@ struct StepScalars {
   uint32_t seed;
 };
 
+// The finalize kernel's total of nb <= 32 partials, from warp 0 alone. In
+// the finalize kernel (norm_total) thread i < nb holds partial i and every
+// other thread 0.0; the first level of the block sum is the shuffle tree of
+// each warp, so warp 0 forms exactly the tree computed here, the other warps
+// form +0.0, and the second level adds only those zeros to warp 0's sum,
+// which changes nothing (x + 0 = x for every partial sum x >= +0, NaN and
+// Inf included). The same bits, with no second level and one barrier.
+template <typename PartialAt>
+__device__ __forceinline__ double small_total(PartialAt partial, int nb, double* sh) {
+  if (threadIdx.x < 32) {
+    double d = static_cast<int>(threadIdx.x) < nb ? __dadd_rn(0.0, partial(threadIdx.x)) : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d = __dadd_rn(d, __shfl_down_sync(0xFFFFFFFFu, d, o));
+    if (threadIdx.x == 0) sh[0] = d;
+  }
+  __syncthreads();
+  return sh[0];
+}
+
 // CTA r updates tile r (if r < n / kTile) and, one element per thread, the
 // tail element n / kTile * kTile + r * kThreads + t (if below n): the
 // general path's mapping for a grid of kSmallClusterCtas blocks when there
@@ -90,8 +109,8 @@ small_step_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Sm
     // 2a. Every CTA adds the partials in the finalize kernel's order (the
     // same total everywhere); CTA 0 records the step. Other CTAs' shared
     // memory is read only here: arrive now, wait before exiting. The arrive
-    // needs no release: every value read has been used by the block sum.
-    const double S = norm_total([&](int i) { return *cluster.map_shared_rank(&partial, i); }, a.nb, sh);
+    // needs no release: every value read has been used by the sum.
+    const double S = small_total([&](int i) { return *cluster.map_shared_rank(&partial, i); }, a.nb, sh);
     __cluster_barrier_arrive_relaxed();
     float norm;
     norm_and_scale(S, a.clip, norm, scale);
@@ -121,7 +140,7 @@ small_step_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Sm
   // derives the norm, records the step, runs the check in the general path's
   // order and hands the scalars to the cluster.
   if (rank == 0) {
-    const double S = norm_total([&](int i) { return *cluster.map_shared_rank(&partial, i); }, a.nb, sh);
+    const double S = small_total([&](int i) { return *cluster.map_shared_rank(&partial, i); }, a.nb, sh);
     if (threadIdx.x == 0) {
       float norm;
       norm_and_scale(S, a.clip, norm, scale);
