@@ -94,6 +94,9 @@ small_step_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Sm
   if (has_tail) load_elem<kMaster>(p, a.norm_src, ti, ein);
   ClockStep cs{0, p.seed, p.bc1, p.bc2, p.lr, true};
   if (a.clock.state != nullptr) cs = next_clock_step(a.clock);
+  Cursor c;  // decay segment of this thread's first element
+  c.s = seg_find(segs, p.nseg, p.goff + (has_tile ? e0 : (has_tail ? ti : p.n - 1)));
+  c.end = segs.end[c.s];
 
   // 1. Norm block `rank` of the general path's grid.
   if (rank < static_cast<uint32_t>(a.nb)) {
@@ -112,23 +115,27 @@ small_step_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Sm
     // needs no release: every value read has been used by the sum.
     const double S = small_total([&](int i) { return *cluster.map_shared_rank(&partial, i); }, a.nb, sh);
     __cluster_barrier_arrive_relaxed();
-    float norm;
-    norm_and_scale(S, a.clip, norm, scale);
-    if (!cs.ok) scale = __int_as_float(0x7FC00000);
-    if (lead) {
-      if (a.clock.state != nullptr) {
-        if (cs.ok) commit_clock_step(a.clock, cs);
-        else if (a.clock.d_status != nullptr) atomicCAS(a.clock.d_status, 0, MP_ERR_RANGE);
+    // One thread takes the fp64 square root (fp64 is a small fraction of the
+    // fp32 rate on this GPU) and shares the scale through shared memory.
+    if (threadIdx.x == 0) {
+      float norm, sc;
+      norm_and_scale(S, a.clip, norm, sc);
+      if (!cs.ok) sc = __int_as_float(0x7FC00000);
+      if (lead) {
+        if (a.clock.state != nullptr) {
+          if (cs.ok) commit_clock_step(a.clock, cs);
+          else if (a.clock.d_status != nullptr) atomicCAS(a.clock.d_status, 0, MP_ERR_RANGE);
+        }
+        *a.d_norm = norm;
+        *a.d_scale = sc;
+        if (!isfinite(sc) && p.d_status != nullptr) atomicCAS(p.d_status, 0, MP_ERR_NONFINITE);
       }
-      *a.d_norm = norm;
-      *a.d_scale = scale;
-      if (!isfinite(scale) && p.d_status != nullptr) atomicCAS(p.d_status, 0, MP_ERR_NONFINITE);
+      out.scale = sc;
     }
+    __syncthreads();
+    scale = out.scale;
     if (isfinite(scale)) {
       const Hyper h{cs.lr, p.beta1, p.beta2, p.eps, p.wd, cs.bc1, cs.bc2};
-      Cursor c;
-      c.s = seg_find(segs, p.nseg, p.goff + (has_tile ? e0 : (has_tail ? ti : p.n - 1)));
-      c.end = segs.end[c.s];
       if (has_tile) update_tile<kMaster>(p, segs, c, e0, tin, scale, h, cs.seed);
       if (has_tail) update_elem<kMaster>(p, segs, c, ti, ein, scale, h, cs.seed);
     }
@@ -168,9 +175,6 @@ small_step_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Sm
   auto token = cluster.barrier_arrive();
   if (isfinite(o.scale)) {
     const Hyper h{o.lr, p.beta1, p.beta2, p.eps, p.wd, o.bc1, o.bc2};
-    Cursor c;
-    c.s = seg_find(segs, p.nseg, p.goff + (has_tile ? e0 : (has_tail ? ti : p.n - 1)));
-    c.end = segs.end[c.s];
     if (has_tile) update_tile<kMaster>(p, segs, c, e0, tin, o.scale, h, o.seed);
     if (has_tail) update_elem<kMaster>(p, segs, c, ti, ein, o.scale, h, o.seed);
   }
