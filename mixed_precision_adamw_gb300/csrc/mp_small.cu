@@ -10,14 +10,14 @@
 // on the norm) and computes one norm partial; at a hardware cluster barrier
 // the partials become visible to the whole cluster, and every CTA reads them
 // out of the other CTAs' shared memory (distributed shared memory) and adds
-// them in the finalize kernel's order, so all CTAs hold the same norm and
-// clip scale and finish their updates with no further barrier; CTA 0 writes
-// the norm, the scale and the step count. With the outlier check, which
+// them with the finalize kernel's bits (small_total), so all CTAs hold the
+// same norm and clip scale and finish their updates with no further
+// barrier; CTA 0 writes the norm, the scale and the step count. With the outlier check, which
 // updates its window in one thread, CTA 0 alone derives the norm, runs the
 // check and hands the scale to the cluster through a second barrier. The
 // results are the general path's bit for bit: CTA r computes the partial of
 // norm block r of the general path's norm grid with the same code
-// (mp_norm.cuh), the partials are added in the finalize kernel's order, and
+// (mp_norm.cuh), the partials are added to the finalize kernel's bits, and
 // the update is the general path's tile and element code (mp_step.cuh). All
 // waits are cluster barriers; the launch co-schedules the cluster's CTAs.
 #include <cooperative_groups.h>
