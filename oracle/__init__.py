@@ -46,6 +46,10 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_stochastic_round.restype = None
     L.oracle_stochastic_round.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64,
                                           ctypes.c_uint64, ctypes.c_uint32]
+    L.oracle_sr_fp16_with_rand.restype = ctypes.c_uint16
+    L.oracle_sr_fp16_with_rand.argtypes = [ctypes.c_float, ctypes.c_uint32]
+    L.oracle_stochastic_round_fp16.restype = None
+    L.oracle_stochastic_round_fp16.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
     L.oracle_accumulate_sr.restype = None
     L.oracle_accumulate_sr.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
     L.oracle_sumsq.restype = ctypes.c_double
@@ -108,6 +112,18 @@ def stochastic_round(x: np.ndarray, global_offset: int, seed: int) -> np.ndarray
     out = np.empty(x.shape, dtype=np.uint16)
     lib().oracle_stochastic_round(_ptr(out, _c_u16p, np.uint16), _ptr(x, _c_f32p, np.float32),
                                   global_offset, x.size, seed)
+    return out
+
+
+def sr_fp16_with_rand(x: float, rand16: int) -> int:
+    return int(lib().oracle_sr_fp16_with_rand(x, rand16))
+
+
+def stochastic_round_fp16(x: np.ndarray, global_offset: int, seed: int) -> np.ndarray:
+    """fp16 patterns (uint16) of the stochastic rounding of fp32 x."""
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_stochastic_round_fp16(_ptr(out, _c_u16p, np.uint16), _ptr(x, _c_f32p, np.float32),
+                                       global_offset, x.size, seed)
     return out
 
 

@@ -95,6 +95,58 @@ void oracle_stochastic_round(uint16_t* out, const float* in,
         out[i] = oracle_sr(in[i], global_offset + i, seed);
 }
 
+/* ---- Stochastic rounding to fp16 -------------------------------------------
+ * [LLMC] §6 notes that fp16 stochastic rounding is unfinished upstream. Read
+ * here as [LLMC] §2.3's rule on fp16's grid: between the fp16 neighbour a
+ * toward zero and the next one b away from zero (b = a + one fp16 step, the
+ * step past the largest finite value giving infinity), round away from zero
+ * when the discarded fraction f = (|x| - |a|) / (|b| - |a|), cut to 16 bits
+ * (floor(f * 65536)), exceeds the 16-bit draw. For fp16 normal values the
+ * fraction has 13 bits, so the rounding is unbiased exactly; for fp16
+ * subnormal values it is cut to 16 bits. Magnitudes of 65536 and above
+ * become infinity (they lie beyond the step after the largest finite fp16),
+ * NaN the canonical quiet NaN 0x7E00; the sign is kept. Computed here in
+ * double from the values, not from bit patterns. */
+static double fp16_value(uint16_t h) /* a finite non-negative pattern */
+{
+    const int e = (h >> 10) & 0x1F;
+    const int m = h & 0x3FF;
+    return e == 0 ? ldexp((double)m, -24) : ldexp(1024.0 + m, e - 25);
+}
+
+uint16_t oracle_sr_fp16_with_rand(float x, uint32_t rand16)
+{
+    if (isnan(x))
+        return 0x7E00u;
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    const double ax = fabs((double)x);
+    if (ax >= 65536.0)
+        return (uint16_t)(sign | 0x7C00u);
+    /* a: the largest fp16 pattern whose value is <= |x| (a binary search over
+     * the ordered non-negative finite patterns 0x0000 .. 0x7BFF) */
+    uint32_t lo = 0, hi = 0x7BFF;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi + 1) / 2;
+        if (fp16_value((uint16_t)mid) <= ax)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const double a = fp16_value((uint16_t)lo);
+    const double step = lo == 0x7BFF ? 32.0 : fp16_value((uint16_t)(lo + 1)) - a;
+    const double f = (ax - a) / step; /* exact: step is a power of two */
+    const uint32_t frac16 = (uint32_t)floor(f * 65536.0);
+    const uint32_t up = frac16 > rand16 ? 1u : 0u;
+    return (uint16_t)(sign | (lo + up)); /* 0x7BFF + 1 = 0x7C00, infinity */
+}
+
+void oracle_stochastic_round_fp16(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n,
+                                  uint32_t seed)
+{
+    for (uint64_t i = 0; i < n; ++i)
+        out[i] = oracle_sr_fp16_with_rand(in[i], oracle_noise_u32(global_offset + i, seed) & 0xFFFFu);
+}
+
 /* ---- Accumulation with stochastic rounding -------------------------------
  * [LLMC] §2.3: the same rounding also writes the embedding gradients of the
  * encoder's backward pass (dwte, dwpe): the stored bf16 gradient is widened

@@ -54,6 +54,11 @@ uint16_t oracle_sr_with_rand(float x, uint32_t rand16);
 uint16_t oracle_sr(float x, uint64_t k, uint32_t seed);
 void oracle_stochastic_round(uint16_t* out, const float* in,
                              uint64_t global_offset, uint64_t n, uint32_t seed);
+/* Stochastic rounding fp32 -> fp16 with a given 16-bit draw, and of a range
+ * keyed on (global index, seed) with the same draws as the bf16 rounding. */
+uint16_t oracle_sr_fp16_with_rand(float x, uint32_t rand16);
+void oracle_stochastic_round_fp16(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n,
+                                  uint32_t seed);
 /* acc[i] = SR((float)acc[i] + delta[i], global_offset + i, seed): a bf16
  * accumulator updated in fp32 and rounded back stochastically. */
 void oracle_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_offset, uint64_t n,

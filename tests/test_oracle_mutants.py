@@ -70,6 +70,12 @@ MUTANTS = {
          "const double sd = sqrt(ss / (ORACLE_OUTLIER_WINDOW - 1));"),
     "outlier: z with the wrong sign":
         ("zz = (x - mean) / sd;", "zz = (mean - x) / sd;"),
+    "fp16: rounds up on a tie with the draw":
+        ("const uint32_t up = frac16 > rand16 ? 1u : 0u;", "const uint32_t up = frac16 >= rand16 ? 1u : 0u;"),
+    "fp16: wrong step past the largest finite value":
+        ("lo == 0x7BFF ? 32.0 :", "lo == 0x7BFF ? 16.0 :"),
+    "fp16: NaN not made canonical":
+        ("    if (isnan(x))\n        return 0x7E00u;", "    if (0)\n        return 0x7E00u;"),
     "accumulate: contribution dropped":
         ("const float sum = bf16_bits_to_float(acc[i]) + delta[i];",
          "const float sum = bf16_bits_to_float(acc[i]);"),
@@ -109,6 +115,11 @@ def _pins():
         ("shards", lambda: P.test_sharded_steps_equal_whole_buffer_steps(True)),
         ("torch AdamW fp64", P.test_sixteen_steps_track_torch_adamw_fp64),
         ("sr tracks small updates", P.test_sr_tracks_small_updates_where_round_to_nearest_stalls),
+        ("fp16 keeps fp16", P.test_sr_fp16_keeps_every_fp16_value),
+        ("fp16 exhaustive", lambda: P.test_sr_fp16_exhaustive_over_draws(1.0 + 2 ** -12)),
+        ("fp16 exhaustive near max", lambda: P.test_sr_fp16_exhaustive_over_draws(65504.5)),
+        ("fp16 half-way", lambda: P.test_sr_fp16_halfway_value_from_the_pages(g)),
+        ("fp16 specials", P.test_sr_fp16_special_values_and_unbiasedness),
         ("accumulate zero", P.test_accumulate_sr_adding_zero_changes_nothing),
         ("accumulate exact", P.test_accumulate_sr_exact_when_the_sum_is_representable),
         ("accumulate unbiased", P.test_accumulate_sr_is_unbiased_over_seeds),

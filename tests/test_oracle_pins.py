@@ -476,6 +476,74 @@ def test_sr_tracks_small_updates_where_round_to_nearest_stalls():
 
 
 # --------------------------------------------------------------------------
+# Stochastic rounding to fp16 — the rule of llm.c ch. 04 §2.3 on fp16's grid
+# (§6: unfinished upstream). The fp16 grid comes from numpy's float16.
+# --------------------------------------------------------------------------
+def _fp16_neighbours(x):
+    """The fp16 values toward zero (a) and away from zero (b) of fp32 x, from
+    numpy's float16 grid."""
+    ax = abs(float(x))
+    with np.errstate(over="ignore"):  # past the largest finite fp16 the neighbour is infinity
+        h = np.float16(ax)  # round to nearest
+        if float(h) > ax:
+            h = np.nextafter(h, np.float16(0))
+        b = np.nextafter(h, np.float16(np.inf))
+    return float(h), float(b)
+
+
+def test_sr_fp16_keeps_every_fp16_value():
+    h = np.arange(0, 0x7C00, dtype=np.uint16)           # every finite non-negative fp16
+    vals = np.concatenate([h.view(np.float16), -h.view(np.float16)]).astype(np.float32)
+    for r in (0, 1, 12345, 65535):
+        got = np.array([oracle.sr_fp16_with_rand(float(v), r) for v in vals[::97]], np.uint16)
+        assert np.array_equal(got.view(np.float16).astype(np.float32), vals[::97])
+
+
+@pytest.mark.parametrize("x", [1.0 + 2 ** -12, 3.14159, -0.1, 1000.3, 65504.5, 65535.9, -65520.0,
+                               1e-5, 3e-8, -1.5e-7, 6.1e-5])
+def test_sr_fp16_exhaustive_over_draws(x):
+    """Over all 65,536 draws the result is one of numpy's two fp16 neighbours
+    and rounds away from zero exactly floor(f * 65536) times."""
+    x = float(np.float32(x))
+    a, b = _fp16_neighbours(x)
+    f = (abs(x) - a) / (b - a) if math.isfinite(b) else (abs(x) - a) / 32.0
+    outs = np.array([oracle.sr_fp16_with_rand(x, r) for r in range(65536)], np.uint16)
+    vals = np.abs(outs.view(np.float16).astype(np.float64))
+    assert set(np.unique(vals).tolist()) <= {a, b}
+    assert int((vals == b).sum()) == math.floor(f * 65536)
+    assert np.all((outs & 0x8000) == (0x8000 if x < 0 else 0))
+    # round-to-nearest (numpy) is one of the two outcomes
+    with np.errstate(over="ignore"):
+        assert abs(float(np.float16(x))) in (a, b)
+
+
+def test_sr_fp16_halfway_value_from_the_pages(golden):
+    """2049 is exactly half-way between the fp16 values 2048 and 2050 ([CMU13]
+    §7.3 ex. 5: 2049 rounds to 2048 in fp16): half of the draws go up."""
+    rows = [r for r in golden("bf16_facts.txt") if r[0] == "fp16" and r[1] == "2049"]
+    assert rows and float(rows[0][2]) == 2048.0
+    outs = [oracle.sr_fp16_with_rand(2049.0, r) for r in range(65536)]
+    assert outs.count(0x6801) == 32768 and outs.count(0x6800) == 32768  # 2050 and 2048
+
+
+def test_sr_fp16_special_values_and_unbiasedness():
+    assert oracle.sr_fp16_with_rand(float("nan"), 3) == 0x7E00
+    assert oracle.sr_fp16_with_rand(float("inf"), 3) == 0x7C00
+    assert oracle.sr_fp16_with_rand(float("-inf"), 3) == 0xFC00
+    assert oracle.sr_fp16_with_rand(0.0, 3) == 0x0000 and oracle.sr_fp16_with_rand(-0.0, 3) == 0x8000
+    for big in (65536.0, 1e6, 3e38):
+        assert oracle.sr_fp16_with_rand(big, 0) == 0x7C00 and oracle.sr_fp16_with_rand(-big, 65535) == 0xFC00
+    # unbiased over 10^5 seeds: 1 + 0.3 fp16 steps
+    x = float(np.float32(1.0 + 0.3 * 2 ** -10))
+    xs = np.full(100_000, x, np.float32)
+    res = np.array([oracle.stochastic_round_fp16(xs[:1], 0, s)[0] for s in range(100_000)], np.uint16)
+    v = res.view(np.float16).astype(np.float64)
+    p = (x - 1.0) / 2 ** -10
+    sigma = 2 ** -10 * math.sqrt(p * (1 - p) / v.size)
+    assert abs(float(v.mean()) - x) < 4 * sigma
+
+
+# --------------------------------------------------------------------------
 # Accumulating into bf16 with stochastic rounding — llm.c ch. 04 §2.3: the
 # same rounding writes the encoder's embedding gradients (a bf16 gradient
 # plus an fp32 contribution, rounded back to bf16).
