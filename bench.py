@@ -363,6 +363,13 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     out["stochastic_round"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
                                "gbs": round(SR_BYTES * N / ms / 1e6, 1),
                                "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
+    # the same rounding onto fp16's grid (into the params buffer, viewed as fp16)
+    h16 = st["params"].view(torch.float16)
+    ms = time_events(lambda: mp.mp_stochastic_round_fp16(h16, st["master"], 7, n=N, stream=stream), iters,
+                     stream)
+    out["stochastic_round_fp16"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
+                                    "gbs": round(SR_BYTES * N / ms / 1e6, 1),
+                                    "frac": round(SR_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": SR_BYTES}
     # bf16 accumulation with stochastic rounding (params += master, in place)
     ms = time_events(lambda: mp.mp_accumulate_sr(st["params"], st["master"], 9, n=N, stream=stream), iters,
                      stream)

@@ -224,6 +224,25 @@ int mp_stochastic_round(uint16_t* out, const float* in,
                         void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Stochastic rounding fp32 -> fp16 of a range. [LLMC] §6 notes that fp16
+ * stochastic rounding is unfinished upstream; this is [LLMC] §2.3's rule on
+ * fp16's grid, with the same draws as the bf16 rounding:
+ *
+ *   out[i] = x's fp16 neighbour toward zero, or the next fp16 away from zero
+ *            when floor(f * 65536) > (noise(global_offset + i, seed) & 0xFFFF),
+ *            f = the discarded fraction of one fp16 step (13 exact bits for
+ *            fp16 normal values; cut to 16 bits below 2^-14)
+ *   |x| >= 65536 -> +-Inf (the step after the largest finite fp16 is Inf);
+ *   NaN -> 0x7E00; the sign is kept.
+ *
+ *   out   fp16[n] patterns (uint16), device, written.   in   fp32[n], device.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_stochastic_round_fp16(uint16_t* out, const float* in,
+                             uint64_t global_offset, uint64_t n, uint32_t seed,
+                             void* stream);
+
+/* ---------------------------------------------------------------------------
  * Accumulation into bf16 with stochastic rounding — [LLMC] §2.3: the same
  * rounding also writes the encoder's embedding gradients in the backward
  * pass (dwte, dwpe): the stored bf16 value is widened to fp32, the fp32

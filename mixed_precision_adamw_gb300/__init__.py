@@ -85,6 +85,8 @@ def _load():
                                 f32, f32, f32, f32, f32, vp, i32, u32, vp, vp]
     L.mp_stochastic_round.restype = ctypes.c_int
     L.mp_stochastic_round.argtypes = [vp, vp, u64, u64, u32, vp]
+    L.mp_stochastic_round_fp16.restype = ctypes.c_int
+    L.mp_stochastic_round_fp16.argtypes = [vp, vp, u64, u64, u32, vp]
     L.mp_accumulate_sr.restype = ctypes.c_int
     L.mp_accumulate_sr.argtypes = [vp, vp, u64, u64, u32, vp]
     L.mp_noise_u32.restype = ctypes.c_int
@@ -244,6 +246,19 @@ def mp_stochastic_round(out: torch.Tensor, inp: torch.Tensor, seed: int, global_
     st = _lib.mp_stochastic_round(_ptr(out, _BF16_LIKE, "out", n), _ptr(inp, (torch.float32,), "in", n),
                                   global_offset, n, seed & 0xFFFFFFFF, _stream(stream))
     _check(st, "mp_stochastic_round")
+
+
+_FP16_LIKE = (torch.float16, torch.int16, torch.uint16)
+
+
+def mp_stochastic_round_fp16(out: torch.Tensor, inp: torch.Tensor, seed: int, global_offset: int = 0,
+                             n: Optional[int] = None, stream=None) -> None:
+    """Enqueue out[i] = fp16 stochastic rounding of inp[i] (draws keyed on
+    global_offset + i and seed, as the bf16 rounding)."""
+    n = inp.numel() if n is None else n
+    st = _lib.mp_stochastic_round_fp16(_ptr(out, _FP16_LIKE, "out", n), _ptr(inp, (torch.float32,), "in", n),
+                                       global_offset, n, seed & 0xFFFFFFFF, _stream(stream))
+    _check(st, "mp_stochastic_round_fp16")
 
 
 def mp_accumulate_sr(acc: torch.Tensor, delta: torch.Tensor, seed: int, global_offset: int = 0,
@@ -503,6 +518,6 @@ __all__ = [
     "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "OutlierDetector", "lib", "abi_version",
     "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
-    "mp_stochastic_round", "mp_accumulate_sr", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
+    "mp_stochastic_round", "mp_stochastic_round_fp16", "mp_accumulate_sr", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
     "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH",
 ]

@@ -432,6 +432,21 @@ int mp_stochastic_round(uint16_t* out, const float* in, uint64_t global_offset, 
   return MP_OK;
 }
 
+int mp_stochastic_round_fp16(uint16_t* out, const float* in, uint64_t global_offset, uint64_t n, uint32_t seed,
+                             void* stream) {
+  if (n == 0) return MP_OK;
+  if (out == nullptr || in == nullptr) return MP_ERR_NULL;
+  if (!aligned(out, 2) || !aligned(in, 4)) return MP_ERR_ALIGN;
+  if (n > kMaxN || global_offset > kMaxN - n) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(in, 16) && aligned(out, 8);
+  e = mpk::launch_sr_fp16(out, in, global_offset, n, seed, vec, dev, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
 int mp_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_offset, uint64_t n, uint32_t seed,
                      void* stream) {
   if (n == 0) return MP_OK;

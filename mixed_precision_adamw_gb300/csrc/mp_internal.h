@@ -136,6 +136,9 @@ cudaError_t launch_outlier_check(void* d_state, const float* d_norm, float z_thr
 cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
                       uint32_t seed, bool vec, const DeviceInfo& dev, cudaStream_t stream);
 
+cudaError_t launch_sr_fp16(uint16_t* out, const float* in, uint64_t goff, uint64_t n, uint32_t seed, bool vec,
+                           const DeviceInfo& dev, cudaStream_t stream);
+
 cudaError_t launch_accumulate_sr(uint16_t* acc, const float* delta, uint64_t goff, uint64_t n, uint32_t seed,
                                  bool vec, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -1,5 +1,6 @@
-// mp_sr.cu — standalone stochastic rounding fp32 -> bf16, accumulation into
-// bf16 with stochastic rounding, and the rounding randomness itself.
+// mp_sr.cu — standalone stochastic rounding fp32 -> bf16 and fp32 -> fp16,
+// accumulation into bf16 with stochastic rounding, and the rounding
+// randomness itself.
 //
 // llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §2.3 (the rule)
 // and §5.2 (bf16 weights are rebuilt from the fp32 master with the saved
@@ -15,6 +16,61 @@ namespace mpk {
 namespace {
 
 constexpr int kSrBlocksPerSm = 8;
+
+// Stochastic rounding fp32 -> fp16: the bf16 rule on fp16's grid. Between
+// the fp16 neighbour toward zero and the next one away from zero, round away
+// when the discarded fraction of one fp16 step, cut to 16 bits, exceeds the
+// 16-bit draw. As for bf16, the work is one 32-bit word v whose high half is
+// the truncated fp16 pattern and whose low half is that 16-bit fraction; then
+// hi16(v + 0xFFFF - draw) carries exactly when the fraction exceeds the draw,
+// and the carry runs into the exponent (0x03FF + 1 is the smallest normal,
+// 0x7BFF + 1 infinity).
+//   fp16 normal range (2^-14 <= |x| < 65536): the fp32 pattern with the
+//     exponent rebiased from 127 to 15, shifted left by 3, so its 10 kept
+//     mantissa bits end at bit 16 and the 13 dropped ones fill bits 15..3.
+//   below 2^-14: v = floor(|x| * 2^40) (fp16 subnormal steps of 2^-24 in the
+//     high half, the fraction in the low), from the 24-bit significand
+//     shifted right by 118 - exponent; a shift of 32 or more (fp32
+//     subnormals included) clamps to 0.
+// Magnitudes from 65536 up become infinity (the step after the largest finite
+// fp16 is infinity), NaN the canonical quiet NaN 0x7E00; the sign is kept.
+// Returns the fp16 pattern in the high half of the word.
+__device__ __forceinline__ uint32_t sr_fp16_hi(float x, uint32_t draw_complement) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t ax = b & 0x7FFFFFFFu;
+  const uint32_t v_normal = (ax - 0x38000000u) << 3;
+  const uint32_t v_sub = __funnelshift_rc((ax << 8) | 0x80000000u, 0u, 118u - (ax >> 23));
+  uint32_t w = (ax >= 0x38800000u ? v_normal : v_sub) + draw_complement;
+  w = ax >= 0x47800000u ? 0x7C000000u : w;
+  w |= b & 0x80000000u;
+  return ax > 0x7F800000u ? 0x7E000000u : w;
+}
+
+// True when 2^-14 <= |x| < 65536 (fp16's normal range), where sr_fp16_hi
+// reduces to sr_fp16_hi_normal.
+__device__ __forceinline__ bool fp16_normal_range(float x) {
+  return (__float_as_uint(x) & 0x7FFFFFFFu) - 0x38800000u < 0x47800000u - 0x38800000u;
+}
+
+// sr_fp16_hi for x in fp16's normal range: (|x| pattern - 0x38000000) << 3
+// is |x| pattern * 8 + 0x40000000 modulo 2^32, and shifting the pattern left
+// by 3 drops the sign bit, so no mask is needed.
+__device__ __forceinline__ uint32_t sr_fp16_hi_normal(float x, uint32_t draw_complement) {
+  const uint32_t b = __float_as_uint(x);
+  return ((b << 3) + 0x40000000u + draw_complement) | (b & 0x80000000u);
+}
+
+// Four consecutive elements at noise positions pos[0..3], packed as fp16.
+template <bool kNormalOnly>
+__device__ __forceinline__ uint2 sr_fp16_pack4(const float4& x, const uint32_t (&pos)[kGroup], uint32_t seed) {
+  auto r = [&](float v, uint32_t p) {
+    return kNormalOnly ? sr_fp16_hi_normal(v, draw16_complement(p, seed)) : sr_fp16_hi(v, draw16_complement(p, seed));
+  };
+  uint2 q;
+  q.x = pack_hi16(r(x.x, pos[0]), r(x.y, pos[1]));
+  q.y = pack_hi16(r(x.z, pos[2]), r(x.w, pos[3]));
+  return q;
+}
 
 // Vector path: in 16-B aligned, out 8-B aligned. Same tiling as the step:
 // thread t converts the 4-element groups at tile offsets 4t and 4t + 1024.
@@ -49,6 +105,51 @@ sr_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint6
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
   for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
     out[i] = static_cast<uint16_t>(sr_bf16_c(in[i], draw16_complement(noise_pos(goff + i), seed)));
+}
+
+// out[i] = fp16 stochastic rounding of in[i] (sr_fp16_hi), with the draws of
+// the bf16 rounding. Vector path: in 16-B aligned, out 8-B aligned.
+__global__ void __launch_bounds__(kThreads, kSrBlocksPerSm)
+sr_fp16_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n,
+                   uint32_t seed) {
+  pdl_enter();
+  const uint64_t ntiles = n / kTile;
+  for (uint64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const uint64_t e0 = tile * kTile + threadIdx.x * kGroup;
+    const uint64_t e1 = e0 + kThreads * kGroup;
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(in + e0));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(in + e1));
+    uint32_t pa[kGroup], pb[kGroup];
+    noise_pos4(goff + e0, pa);
+    noise_pos4(goff + e1, pb);
+    // Warps whose 256 elements all lie in fp16's normal range (the usual
+    // case for weights) take the short form; the vote keeps warps converged.
+    const bool normal = fp16_normal_range(a.x) & fp16_normal_range(a.y) & fp16_normal_range(a.z) &
+                        fp16_normal_range(a.w) & fp16_normal_range(b.x) & fp16_normal_range(b.y) &
+                        fp16_normal_range(b.z) & fp16_normal_range(b.w);
+    uint2 qa, qb;
+    if (__all_sync(0xFFFFFFFFu, normal)) {
+      qa = sr_fp16_pack4<true>(a, pa, seed);
+      qb = sr_fp16_pack4<true>(b, pb, seed);
+    } else {
+      qa = sr_fp16_pack4<false>(a, pa, seed);
+      qb = sr_fp16_pack4<false>(b, pb, seed);
+    }
+    __stcs(reinterpret_cast<uint2*>(out + e0), qa);
+    __stcs(reinterpret_cast<uint2*>(out + e1), qb);
+  }
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = ntiles * kTile + static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint16_t>(sr_fp16_hi(in[i], draw16_complement(noise_pos(goff + i), seed)) >> 16);
+}
+
+__global__ void __launch_bounds__(kThreads)
+sr_fp16_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n,
+                      uint32_t seed) {
+  pdl_enter();
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n; i += stride)
+    out[i] = static_cast<uint16_t>(sr_fp16_hi(in[i], draw16_complement(noise_pos(goff + i), seed)) >> 16);
 }
 
 // acc[i] = SR((float)acc[i] + delta[i], goff + i, seed), in place. Vector
@@ -122,6 +223,16 @@ cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n,
     return launch_pdl(sr_vec_kernel, blocks, kThreads, stream, out, in, goff, n, seed);
   }
   return launch_pdl(sr_scalar_kernel, grid_for(n, dev), kThreads, stream, out, in, goff, n, seed);
+}
+
+cudaError_t launch_sr_fp16(uint16_t* out, const float* in, uint64_t goff, uint64_t n, uint32_t seed, bool vec,
+                           const DeviceInfo& dev, cudaStream_t stream) {
+  if (vec) {
+    const uint64_t ntiles = n / kTile;
+    const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);
+    return launch_pdl(sr_fp16_vec_kernel, blocks, kThreads, stream, out, in, goff, n, seed);
+  }
+  return launch_pdl(sr_fp16_scalar_kernel, grid_for(n, dev), kThreads, stream, out, in, goff, n, seed);
 }
 
 cudaError_t launch_accumulate_sr(uint16_t* acc, const float* delta, uint64_t goff, uint64_t n, uint32_t seed,

@@ -101,6 +101,12 @@ def test_norm_and_sr_argument_checks(mp):
     assert L.mp_stochastic_round(FAKE, FAKE + 2, 0, 10, 1, None) == mp.MP_ERR_ALIGN
     assert L.mp_stochastic_round(FAKE, FAKE, (1 << 62), 10, 1, None) == mp.MP_ERR_RANGE
     assert L.mp_stochastic_round(FAKE, FAKE, 0, 0, 1, None) == mp.MP_OK
+    assert L.mp_stochastic_round_fp16(None, FAKE, 0, 10, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_stochastic_round_fp16(FAKE, None, 0, 10, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_stochastic_round_fp16(FAKE + 1, FAKE, 0, 10, 1, None) == mp.MP_ERR_ALIGN
+    assert L.mp_stochastic_round_fp16(FAKE, FAKE + 2, 0, 10, 1, None) == mp.MP_ERR_ALIGN
+    assert L.mp_stochastic_round_fp16(FAKE, FAKE, (1 << 62), 10, 1, None) == mp.MP_ERR_RANGE
+    assert L.mp_stochastic_round_fp16(FAKE, FAKE, 0, 0, 1, None) == mp.MP_OK
     assert L.mp_accumulate_sr(None, FAKE, 0, 10, 1, None) == mp.MP_ERR_NULL
     assert L.mp_accumulate_sr(FAKE, None, 0, 10, 1, None) == mp.MP_ERR_NULL
     assert L.mp_accumulate_sr(FAKE + 1, FAKE, 0, 10, 1, None) == mp.MP_ERR_ALIGN

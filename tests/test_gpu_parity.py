@@ -129,6 +129,97 @@ def test_accumulate_sr_bit_exact(n, pad_acc, pad_delta, goff):
     assert_bit_equal(to_np_u16(acc), ref, "accumulate_sr")
 
 
+def _fp16_cases(n, rng):
+    """fp32 inputs for the fp16 rounding: the specials of the bf16 tests, the
+    fp16 boundaries (subnormal/normal at 2^-14, the largest finite 65504, the
+    overflow edge 65536, fp16's smallest subnormal 2^-24 and below), values
+    just off every fp16 exponent, and magnitudes spread over fp16's range."""
+    x = _special_f32(n, rng)
+    with np.errstate(over="ignore"):
+        x[n // 4: n // 2] = (rng.standard_normal(n // 2 - n // 4) *
+                             2.0 ** rng.uniform(-30, 17, n // 2 - n // 4)).astype(np.float32)
+    edges = [2.0 ** -14, 2.0 ** -24, 2.0 ** -25, 2.0 ** -26, 65504.0, 65519.99, 65520.0, 65535.99, 65536.0,
+             65537.0, 1e5, 6.1e-5, 5.96e-8, 3e-8, 1.0, 0.5, 1024.0 + 0.5, 2048.0 + 1.0]
+    edges += [2.0 ** e for e in range(-24, 16)]
+    e = np.array(edges, np.float32)
+    near = np.concatenate([e, np.nextafter(e, np.float32(0)), np.nextafter(e, np.float32(np.inf))])
+    near = np.concatenate([near, -near])
+    x[16:16 + near.size] = near
+    return x
+
+
+@pytest.mark.parametrize("n,pad_in,pad_out,goff", [
+    (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32),
+    (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000),
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5001), (2048 * 7 + 5, 0, 0, (1 << 32) - 5003),
+    ((1 << 22) + 3, 0, 0, 123)])
+def test_stochastic_round_fp16_bit_exact(n, pad_in, pad_out, goff):
+    """fp32 -> fp16 stochastic rounding, bit-exact against the oracle: fp16
+    subnormals, the subnormal/normal boundary, 65504 .. 65536 and beyond,
+    NaN, Inf, signed zeros; vector and scalar paths; offsets across 2^32."""
+    rng = np.random.default_rng(3 * n + pad_out)
+    x = _fp16_cases(n, rng) if n > 2000 else rng.standard_normal(n).astype(np.float32)
+    xin = dev_f32(x, pad_in)
+    buf = torch.zeros(n + pad_out, dtype=torch.float16, device=DEV)
+    out = buf[pad_out:]
+    seed = 0xF16
+    mp.mp_stochastic_round_fp16(out, xin, seed, global_offset=goff)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_bit_equal(got, oracle.stochastic_round_fp16(x, goff, seed), "sr fp16")
+
+
+@pytest.mark.parametrize("goff", [0, (1 << 32) - 3001])
+def test_stochastic_round_fp16_weights_and_scattered_specials(goff):
+    """Weight-like values (N(0, 0.02), all in fp16's normal range) over many
+    tiles and a ragged tail, then the same with one zero, subnormal, NaN or
+    overflow scattered into some warps' elements: every warp shape of the
+    vector kernel (all normal, some special) is bit-exact against the oracle."""
+    n = 2048 * 300 + 777
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    x = np.where(np.abs(x) < 2.0 ** -13, np.float32(0.5), x).astype(np.float32)
+    for special_every in (None, 9973):
+        if special_every is not None:
+            idx = np.arange(17, n, special_every)
+            x[idx] = np.resize(np.array([0.0, -1e-6, np.nan, -7e4, 3e-9, np.inf, 65519.99], np.float32), idx.size)
+        out = torch.empty(n, dtype=torch.float16, device=DEV)
+        mp.mp_stochastic_round_fp16(out, dev_f32(x), 0x5EED, global_offset=goff)
+        got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        assert_bit_equal(got, oracle.stochastic_round_fp16(x, goff, 0x5EED), f"sr fp16 specials {special_every}")
+
+
+def test_stochastic_round_fp16_every_pattern_and_unbiased():
+    """Every finite fp16 pattern round-trips unchanged; values between two
+    fp16 neighbours land on one of them and average to the input over many
+    seeds (float64 mean over 4096 draws per value)."""
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = h.view(np.float16)
+    keep = np.isfinite(vals)
+    x = vals[keep].astype(np.float32)
+    out = torch.empty(x.size, dtype=torch.float16, device=DEV)
+    mp.mp_stochastic_round_fp16(out, dev_f32(x), 99)
+    assert_bit_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), h[keep], "fp16 round trip")
+
+    rng = np.random.default_rng(5)
+    lo = np.concatenate([np.arange(1, 1023, 37), np.arange(0x3C00, 0x3C40), np.arange(0x7B80, 0x7BFF, 7)])
+    lo = lo.astype(np.uint16)
+    a = lo.view(np.float16).astype(np.float64)
+    b = (lo + 1).view(np.float16).astype(np.float64)
+    t = rng.uniform(0.05, 0.95, lo.size)
+    x = (a + t * (b - a)).astype(np.float32)
+    reps = 4096
+    xs = torch.from_numpy(np.tile(x, reps)).to(DEV)
+    out = torch.empty(xs.numel(), dtype=torch.float16, device=DEV)
+    mp.mp_stochastic_round_fp16(out, xs, 1234)
+    r = out.view(reps, lo.size)
+    bits = r.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.all((bits == lo) | (bits == lo + 1))
+    mean = r.double().mean(0).cpu().numpy()
+    p = (x.astype(np.float64) - a) / (b - a)
+    tol = 5.0 * np.sqrt(p * (1 - p) / reps) * (b - a) + 1e-12
+    assert np.all(np.abs(mean - x.astype(np.float64)) <= tol)
+
+
 def test_stochastic_round_full_size_and_drift():
     """SR stress: 64M fp32 weights with |w| log-uniform in [1e-3, 1e1]; a
     constant update of 1e-4 |w| per step for 1000 steps. SR (bit-exact
