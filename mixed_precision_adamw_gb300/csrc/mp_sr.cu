@@ -24,32 +24,35 @@ constexpr int kSrBlocksPerSm = 8;
 // the truncated fp16 pattern and whose low half is that 16-bit fraction; then
 // hi16(v + 0xFFFF - draw) carries exactly when the fraction exceeds the draw,
 // and the carry runs into the exponent (0x03FF + 1 is the smallest normal,
-// 0x7BFF + 1 infinity).
-//   fp16 normal range (2^-14 <= |x| < 65536): the fp32 pattern with the
-//     exponent rebiased from 127 to 15, shifted left by 3, so its 10 kept
-//     mantissa bits end at bit 16 and the 13 dropped ones fill bits 15..3.
-//   below 2^-14: v = floor(|x| * 2^40) (fp16 subnormal steps of 2^-24 in the
-//     high half, the fraction in the low), from the 24-bit significand
-//     shifted right by 118 - exponent; a shift of 32 or more (fp32
-//     subnormals included) clamps to 0.
-// Magnitudes from 65536 up become infinity (the step after the largest finite
-// fp16 is infinity), NaN the canonical quiet NaN 0x7E00; the sign is kept.
+// 0x7BFF + 1 infinity). Two candidate words, of which v is the smaller:
+//   v_normal: the pattern of |x| clamped to [2^-14, 65536], rebiased from
+//     127 to 15 and shifted left by 3 (pattern * 8 + 0x40000000 modulo
+//     2^32), so the 10 kept mantissa bits end at bit 16 and the 13 dropped
+//     ones fill bits 15..3. Exact for 2^-14 <= |x| < 65536; 0x7C000000
+//     (infinity, no carry possible) from 65536 up; 2^26 below 2^-14.
+//   v_sub: floor(|x| * 2^40) (the product is exact; the conversion truncates
+//     and saturates at 2^32 - 1), fp16 subnormal steps of 2^-24 in the high
+//     half and the fraction in the low. Exact below 2^-14, where it is below
+//     2^26; from 2^-14 up it is never below v_normal (the linear scale grows
+//     at least as fast as the exponent-and-mantissa one, and they meet at
+//     2^-14).
+// NaN gives the canonical quiet NaN 0x7E00; otherwise the sign is kept.
+// The conversion and the multiplies run on the FMA and conversion pipes,
+// which this integer-heavy kernel leaves mostly idle.
 // Returns the fp16 pattern in the high half of the word.
 __device__ __forceinline__ uint32_t sr_fp16_hi(float x, uint32_t draw_complement) {
-  const uint32_t b = __float_as_uint(x);
-  const uint32_t ax = b & 0x7FFFFFFFu;
-  const uint32_t v_normal = (ax - 0x38000000u) << 3;
-  const uint32_t v_sub = __funnelshift_rc((ax << 8) | 0x80000000u, 0u, 118u - (ax >> 23));
-  uint32_t w = (ax >= 0x38800000u ? v_normal : v_sub) + draw_complement;
-  w = ax >= 0x47800000u ? 0x7C000000u : w;
-  w |= b & 0x80000000u;
-  return ax > 0x7F800000u ? 0x7E000000u : w;
+  const float a = fabsf(x);
+  const uint32_t v_normal = __float_as_uint(fminf(fmaxf(a, 0x1p-14f), 65536.0f)) * 8u + 0x40000000u;
+  const uint32_t v_sub = __float2uint_rz(__fmul_rn(a, 0x1p40f));
+  const uint32_t w = (min(v_normal, v_sub) + draw_complement) | (__float_as_uint(x) & 0x80000000u);
+  return x != x ? 0x7E000000u : w;
 }
 
 // True when 2^-14 <= |x| < 65536 (fp16's normal range), where sr_fp16_hi
-// reduces to sr_fp16_hi_normal.
+// reduces to sr_fp16_hi_normal. Doubling the pattern drops the sign bit; the
+// range is then [0x71000000, 0x8F000000), tested with one unsigned compare.
 __device__ __forceinline__ bool fp16_normal_range(float x) {
-  return (__float_as_uint(x) & 0x7FFFFFFFu) - 0x38800000u < 0x47800000u - 0x38800000u;
+  return __float_as_uint(x) * 2u - 0x71000000u < 0x1E000000u;
 }
 
 // sr_fp16_hi for x in fp16's normal range: (|x| pattern - 0x38000000) << 3
@@ -122,19 +125,13 @@ sr_fp16_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uin
     uint32_t pa[kGroup], pb[kGroup];
     noise_pos4(goff + e0, pa);
     noise_pos4(goff + e1, pb);
-    // Warps whose 256 elements all lie in fp16's normal range (the usual
-    // case for weights) take the short form; the vote keeps warps converged.
-    const bool normal = fp16_normal_range(a.x) & fp16_normal_range(a.y) & fp16_normal_range(a.z) &
-                        fp16_normal_range(a.w) & fp16_normal_range(b.x) & fp16_normal_range(b.y) &
-                        fp16_normal_range(b.z) & fp16_normal_range(b.w);
-    uint2 qa, qb;
-    if (__all_sync(0xFFFFFFFFu, normal)) {
-      qa = sr_fp16_pack4<true>(a, pa, seed);
-      qb = sr_fp16_pack4<true>(b, pb, seed);
-    } else {
-      qa = sr_fp16_pack4<false>(a, pa, seed);
-      qb = sr_fp16_pack4<false>(b, pb, seed);
-    }
+    // Per group set (a: groups 4t, b: groups 4t + 1024): a warp whose 128
+    // elements all lie in fp16's normal range takes the short form; the
+    // vote keeps the warp converged.
+    const bool na = fp16_normal_range(a.x) & fp16_normal_range(a.y) & fp16_normal_range(a.z) & fp16_normal_range(a.w);
+    const bool nb = fp16_normal_range(b.x) & fp16_normal_range(b.y) & fp16_normal_range(b.z) & fp16_normal_range(b.w);
+    const uint2 qa = __all_sync(0xFFFFFFFFu, na) ? sr_fp16_pack4<true>(a, pa, seed) : sr_fp16_pack4<false>(a, pa, seed);
+    const uint2 qb = __all_sync(0xFFFFFFFFu, nb) ? sr_fp16_pack4<true>(b, pb, seed) : sr_fp16_pack4<false>(b, pb, seed);
     __stcs(reinterpret_cast<uint2*>(out + e0), qa);
     __stcs(reinterpret_cast<uint2*>(out + e1), qb);
   }
