@@ -5,7 +5,8 @@
  *
  * One optimizer step (mp_optimizer_step, then a second call of the pieces:
  * mp_grad_norm + mp_adamw_step) on n = 100,003 elements split into 7 tensors
- * with alternating decay flags, then mp_stochastic_round and mp_accumulate_sr.
+ * with alternating decay flags, then mp_stochastic_round, mp_accumulate_sr and
+ * mp_stochastic_round_fp16.
  * Then steps 3-6 as replayable steps: step 3 a plain mp_optimizer_step_graph
  * call, steps 4-6 replays of one CUDA graph captured from a stream, with
  * fresh gradients copied in between. Exit status 0 when every output is
@@ -53,7 +54,7 @@ static int same(const void* a, const void* b, size_t bytes, const char* what) {
 }
 
 int main(void) {
-    static uint16_t params[N], grads[N], params_o[N], out_sr[N], out_sr_o[N];
+    static uint16_t params[N], grads[N], params_o[N], out_sr[N], out_sr_o[N], out_h[N], out_h_o[N];
     static float master[N], m[N], v[N], master_o[N], m_o[N], v_o[N];
     for (uint32_t i = 0; i < N; ++i) {
         master[i] = 0.05f * rng_uniform();
@@ -76,7 +77,7 @@ int main(void) {
     memcpy(m_o, m, sizeof m);
     memcpy(v_o, v, sizeof v);
 
-    uint16_t *d_params, *d_grads, *d_sr;
+    uint16_t *d_params, *d_grads, *d_sr, *d_h;
     float *d_master, *d_m, *d_v, *d_norm, *d_scale;
     int32_t* d_status;
     void* d_ws;
@@ -84,6 +85,7 @@ int main(void) {
     CK(cudaMalloc((void**)&d_params, sizeof params));
     CK(cudaMalloc((void**)&d_grads, sizeof grads));
     CK(cudaMalloc((void**)&d_sr, sizeof out_sr));
+    CK(cudaMalloc((void**)&d_h, sizeof out_h));
     CK(cudaMalloc((void**)&d_master, sizeof master));
     CK(cudaMalloc((void**)&d_m, sizeof m));
     CK(cudaMalloc((void**)&d_v, sizeof v));
@@ -114,6 +116,7 @@ int main(void) {
     /* standalone rounding of the new master, then accumulating the master into it */
     MP(mp_stochastic_round(d_sr, d_master, 0, N, 99, NULL));
     MP(mp_accumulate_sr(d_sr, d_master, 0, N, 98, NULL));
+    MP(mp_stochastic_round_fp16(d_h, d_master, 0, N, 97, NULL));
     int32_t status;
     CK(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(params, d_params, sizeof params, cudaMemcpyDeviceToHost));
@@ -121,6 +124,7 @@ int main(void) {
     CK(cudaMemcpy(m, d_m, sizeof m, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(v, d_v, sizeof v, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(out_sr, d_sr, sizeof out_sr, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(out_h, d_h, sizeof out_h, cudaMemcpyDeviceToHost));
 
     /* the oracle, with the GPU's clip scales (the norms are checked to 1e-6) */
     double sumsq;
@@ -137,12 +141,14 @@ int main(void) {
         return 1;
     oracle_stochastic_round(out_sr_o, master_o, 0, N, 99);
     oracle_accumulate_sr(out_sr_o, master_o, 0, N, 98);
+    oracle_stochastic_round_fp16(out_h_o, master_o, 0, N, 97);
     int ok = status == 0;
     ok &= same(params, params_o, sizeof params, "params");
     ok &= same(master, master_o, sizeof master, "master");
     ok &= same(m, m_o, sizeof m, "m");
     ok &= same(v, v_o, sizeof v, "v");
     ok &= same(out_sr, out_sr_o, sizeof out_sr, "stochastic round + accumulate");
+    ok &= same(out_h, out_h_o, sizeof out_h, "fp16 stochastic round");
 
     /* steps 3..6 with the step count on the device: seed of step t = 10 + t */
     enum { FIRST = 3, LAST = 6 };
@@ -217,7 +223,7 @@ int main(void) {
            ok ? "bit-identical to the oracle" : "MISMATCH", N, norm1, scale1, FIRST, LAST);
     cudaGraphExecDestroy(exec); cudaGraphDestroy(graph); cudaStreamDestroy(stream); free(bias);
     cudaFree(d_bias); cudaFree(d_state);
-    cudaFree(d_params); cudaFree(d_grads); cudaFree(d_sr); cudaFree(d_master); cudaFree(d_m); cudaFree(d_v);
+    cudaFree(d_params); cudaFree(d_grads); cudaFree(d_sr); cudaFree(d_h); cudaFree(d_master); cudaFree(d_m); cudaFree(d_v);
     cudaFree(d_norm); cudaFree(d_scale); cudaFree(d_status); cudaFree(d_ws);
     return ok ? 0 : 1;
 }

@@ -2,8 +2,8 @@
 the update over a range (random sizes, global offsets up to 5·2^32, tables
 of 1 to 2^20-element tensors, unaligned buffers, both variants, betas,
 eps, lr, decay and step counts), the whole-step call (cluster kernel below
-32,768 params, the general path above), the standalone rounding and the
-accumulate-and-round, on values from 1e-40 to 1e38."""
+32,768 params, the general path above), the standalone rounding to bf16
+and to fp16 and the accumulate-and-round, on values from 1e-40 to 1e38."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +18,7 @@ if torch.cuda.is_available():
     __graft_entry__.build()
     import mixed_precision_adamw_gb300 as mp
 
-CASES = 160
+CASES = 200
 
 
 @pytest.fixture(autouse=True)
@@ -99,9 +99,9 @@ def _update_case(rng, whole):
 
 def test_random_sweep_against_the_oracle():
     rng = np.random.default_rng(20261202)
-    counts = dict(step=0, whole=0, sr=0, acc=0)
+    counts = dict(step=0, whole=0, sr=0, acc=0, sr16=0)
     for _ in range(CASES):
-        kind = str(rng.choice(["step", "whole", "sr", "acc"]))
+        kind = str(rng.choice(["step", "whole", "sr", "acc", "sr16"]))
         counts[kind] += 1
         if kind in ("step", "whole"):
             _update_case(rng, kind == "whole")
@@ -115,6 +115,10 @@ def test_random_sweep_against_the_oracle():
             out = _dev16(np.zeros(n, np.uint16), pad)
             mp.mp_stochastic_round(out, _dev32(x, pad_in), seed, global_offset=goff)
             assert np.array_equal(_u16(out), oracle.stochastic_round(x, goff, seed)), (n, goff, pad)
+        elif kind == "sr16":
+            out = _dev16(np.zeros(n, np.uint16), pad)
+            mp.mp_stochastic_round_fp16(out.view(torch.float16), _dev32(x, pad_in), seed, global_offset=goff)
+            assert np.array_equal(_u16(out), oracle.stochastic_round_fp16(x, goff, seed)), (n, goff, pad)
         else:
             acc0 = rng.integers(0, 1 << 16, n, dtype=np.uint32).astype(np.uint16)
             acc = _dev16(acc0, pad)
