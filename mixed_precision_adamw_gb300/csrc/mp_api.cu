@@ -1,6 +1,7 @@
 // mp_api.cu — the C ABI declared in include/mp_adamw.h: argument checks,
 // host-side scalars (bias corrections, decay segments) and kernel launches.
 // Nothing here synchronises, allocates device memory, prints or exits.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <vector>
@@ -37,15 +38,15 @@ constexpr int64_t kMaxBiasLen = int64_t{1} << 26;
 namespace mpk {
 
 cudaError_t device_info(DeviceInfo* out) {
-  static int sms_cache[64];  // 0 = not yet queried
+  static std::atomic<int> sms_cache[64];  // 0 = not yet queried; racing callers store the same value
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+  int sms = (dev >= 0 && dev < 64) ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
   if (sms == 0) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+    if (dev >= 0 && dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
   }
   out->device = dev;
   out->sms = sms;

@@ -22,6 +22,7 @@
 // waits are cluster barriers; the launch co-schedules the cluster's CTAs.
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "mp_adamw.h"
@@ -203,9 +204,10 @@ cudaLaunchConfig_t small_config(cudaLaunchAttribute (&attr)[2], cudaStream_t str
 // -1 = no; racing first calls store the same answer.
 template <bool kMaster>
 bool available(int device) {
-  static int answer[64];
+  static std::atomic<int> answer[64];
   if (device < 0 || device >= 64) return false;
-  if (answer[device] == 0) {
+  int known = answer[device].load(std::memory_order_relaxed);
+  if (known == 0) {
     int size = 0;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = small_config(attr, nullptr);
@@ -215,9 +217,10 @@ bool available(int device) {
               cudaOccupancyMaxPotentialClusterSize(&size, small_step_kernel<kMaster>, &cfg) == cudaSuccess &&
               size >= kSmallClusterCtas;
     if (!ok) cudaGetLastError();  // clear a non-sticky error of the queries
-    answer[device] = ok ? 1 : -1;
+    known = ok ? 1 : -1;
+    answer[device].store(known, std::memory_order_relaxed);
   }
-  return answer[device] > 0;
+  return known > 0;
 }
 
 }  // namespace

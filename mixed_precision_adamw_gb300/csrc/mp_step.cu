@@ -8,6 +8,7 @@
 // arrays in one pass, in a grid-stride loop of persistent blocks sized to the
 // SM count. Weight decay comes from a per-launch table of decay segments
 // (maximal runs of tensors with equal decay flag, §2.2's "2D tensors only").
+#include <atomic>
 #include <cmath>
 
 #include "mp_device.cuh"
@@ -60,12 +61,15 @@ adamw_scalar_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ 
 // belong to that one kernel: the with- and no-master instantiations share a
 // function-pointer type but not their register counts.
 template <typename K>
-int blocks_per_sm(K kernel, int device, int (&cache)[64]) {
-  if (device < 0 || device >= 64) device = 0;
-  int nb = cache[device];  // 0 = not yet queried; racing writers store the same value
+int blocks_per_sm(K kernel, int device, std::atomic<int> (&cache)[64]) {
+  const bool cached = device >= 0 && device < 64;
+  int nb = cached ? cache[device].load(std::memory_order_relaxed) : 0;  // 0 = not yet queried
   if (nb == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess || nb < 1) nb = 1;
-    cache[device] = nb;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kThreads, 0) != cudaSuccess || nb < 1) {
+      cudaGetLastError();  // clear the query's error; the launch reports its own
+      return 1;            // not cached: the next call asks again
+    }
+    if (cached) cache[device].store(nb, std::memory_order_relaxed);  // racing callers store the same value
   }
   return nb;
 }
@@ -76,7 +80,7 @@ cudaError_t launch_cap(const StepArgs& a, const uint64_t* seg_end, bool vec, con
   SegTable<CAP> t;
   for (uint32_t s = 0; s < a.nseg; ++s) t.end[s] = seg_end[s];
   for (uint32_t s = a.nseg; s < CAP; ++s) t.end[s] = seg_end[a.nseg - 1];
-  static int vec_occupancy[64], scalar_occupancy[64];  // one cache per <kMaster, CAP, kDev> kernel
+  static std::atomic<int> vec_occupancy[64], scalar_occupancy[64];  // one cache per <kMaster, CAP, kDev> kernel
   const uint64_t ntiles = a.n / kTile;
   if (vec) {
     auto k = adamw_vec_kernel<kMaster, CAP, kDev>;
