@@ -113,3 +113,98 @@ def test_fp16_rounding_keeps_values_on_the_grid(h, draw):
 def test_fp16_rounding_past_the_range_is_infinity(x, neg, draw):
     v = -x if neg else x
     assert oracle.sr_fp16_with_rand(v, draw) == (0xFC00 if neg else 0x7C00)
+
+
+# --------------------------------------------------------------------------
+# One AdamW step with drawn hyperparameters against torch.optim.AdamW in
+# float64 (llm.c walk-through ch. 04 §2.2: m and v as lerps, bias-corrected
+# moments, decoupled decay on decay-flagged tensors, the clip scale on the
+# gradient). The bound is fp32 rounding of each operation of the step, taken
+# from the float64 reference values, with a factor 4 of slack. The betas are
+# 0 or at least 1e-4: torch forms m as m0 + (1 - beta1)(g - m0), and below
+# 2^-53 the float64 1 - beta1 is exactly 1, dropping beta1 * m0 from its
+# reference.
+# --------------------------------------------------------------------------
+U = 2.0 ** -24
+
+
+def _log_uniform(lo, hi):
+    return st.floats(min_value=math.log10(lo), max_value=math.log10(hi)).map(lambda e: 10.0 ** e)
+
+
+def _f32(x):
+    return float(np.float32(x))
+
+
+@settings(max_examples=300, deadline=None)
+@given(b1=st.one_of(st.just(0.0), st.floats(1e-4, 0.999)), b2=st.one_of(st.just(0.0), st.floats(1e-4, 0.9999)),
+       lr=_log_uniform(1e-6, 1.0),
+       eps=_log_uniform(1e-10, 1e-2), wd=st.floats(0.0, 1.0), t=st.integers(1, 100000),
+       scale=st.floats(0.01, 1.0), decay=st.booleans(), master=st.booleans(), seed=st.integers(0, 2 ** 32 - 1))
+def test_one_step_tracks_torch_adamw_fp64(b1, b2, lr, eps, wd, t, scale, decay, master, seed):
+    b1, b2, lr, eps, wd, scale = (_f32(x) for x in (b1, b2, lr, eps, wd, scale))
+    rng = np.random.default_rng(seed)
+    n = 256
+    sign = lambda: rng.choice([-1.0, 1.0], n)  # noqa: E731
+    g32 = (sign() * 10.0 ** rng.uniform(-6, 2, n)).astype(np.float32)
+    g32[:8] = 0.0
+    gbits = W_bf16(g32)
+    g = (gbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    old32 = (sign() * 10.0 ** rng.uniform(-3, 3, n)).astype(np.float32)
+    pbits = W_bf16(old32)
+    if not master:
+        old32 = (pbits.astype(np.uint32) << 16).view(np.float32)
+    m0 = (sign() * 10.0 ** rng.uniform(-6, 2, n)).astype(np.float32)
+    v0 = (10.0 ** rng.uniform(-12, 4, n)).astype(np.float32)
+    ms, m, v, params = old32.copy(), m0.copy(), v0.copy(), pbits.copy()
+    assert oracle.adamw_step(params, gbits.copy(), ms if master else None, m, v, 0, [(0, n, int(decay))],
+                             lr, b1, b2, eps, wd, scale, t, 11) == 0
+
+    wd_e = wd if decay else 0.0
+    p = torch.nn.Parameter(torch.from_numpy(old32.astype(np.float64)))
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd_e, foreach=False)
+    opt.state[p] = {"step": torch.tensor(float(t - 1)), "exp_avg": torch.from_numpy(m0.astype(np.float64)),
+                    "exp_avg_sq": torch.from_numpy(v0.astype(np.float64))}
+    p.grad = torch.from_numpy(g * scale)
+    opt.step()
+    p_ref = p.detach().numpy()
+    m_ref = opt.state[p]["exp_avg"].numpy()
+    v_ref = opt.state[p]["exp_avg_sq"].numpy()
+
+    old = old32.astype(np.float64)
+    gs = np.abs(g * scale)
+    DN = 2.0 ** -149  # fp32 subnormal spacing: the absolute error floor of each operation
+    dm = 2 * U * (b1 * np.abs(m0) + (1 - b1) * gs) + U * (1 - b1) * gs + 2 * DN
+    dv = 5 * U * (b2 * v0 + (1 - b2) * gs * gs) + 2 * DN
+    bc1, bc2 = 1 - b1 ** t, 1 - b2 ** t
+    m_hat, v_hat = m_ref / bc1, v_ref / bc2
+    dmh = dm / bc1 + 2 * U * np.abs(m_hat) + DN
+    dvh = dv / bc2 + 2 * U * v_hat + DN
+    sq = np.sqrt(v_hat)
+    with np.errstate(divide="ignore"):
+        dsq = np.minimum(np.sqrt(dvh), np.where(sq > 0, dvh / (2 * sq), np.inf)) + U * sq
+    d = sq + eps
+    dd = dsq + U * d
+    u = m_hat / d
+    du = dmh / d + np.abs(u) * dd / d + U * np.abs(u) + DN
+    term = u + wd_e * old
+    dterm = du + U * wd_e * np.abs(old) + U * np.abs(term) + DN
+    dp = U * np.abs(p_ref) + lr * dterm + U * lr * np.abs(term) + U * np.abs(old) + DN
+
+    def worst(err, bound):
+        return float((err / bound).max())
+
+    assert (np.abs(m - m_ref) <= 4 * dm).all(), worst(np.abs(m - m_ref), dm)
+    assert (np.abs(v - v_ref) <= 4 * dv).all(), worst(np.abs(v - v_ref), dv)
+    if master:
+        err = np.abs(ms.astype(np.float64) - p_ref)
+        assert (err <= 4 * dp).all(), worst(err, dp)
+    # the bf16 weight is within one bf16 step of the fp32 result
+    pf = (params.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(p_ref), 1e-30))) - 7)
+    assert (np.abs(pf - p_ref) <= ulp * (1 + 1e-6) + 4 * dp).all()
+
+
+def W_bf16(x32: np.ndarray) -> np.ndarray:
+    """bf16 patterns of fp32 values by torch's round-to-nearest cast."""
+    return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
