@@ -256,6 +256,40 @@ def test_stochastic_round_full_size_and_drift():
     assert abs(drift_sr) < 1e-4, drift_sr
 
 
+def test_stochastic_round_fp16_full_size_and_drift():
+    """The SR-stress workload rounded to fp16: 64M fp32 weights, |w|
+    log-uniform in [1e-3, 10] (all in fp16's normal range), bit-exact against
+    the oracle in windows at both ends and in the middle; then a constant
+    update of 1e-4 |w| per step (below half an fp16 step) for 1000 steps.
+    fp16 stochastic rounding tracks the fp32 trajectory; round-to-nearest
+    never moves."""
+    n = 64 << 20
+    w0 = W.sr_stress_weights(n, device=DEV)
+    out = torch.empty(n, dtype=torch.float16, device=DEV)
+    mp.mp_stochastic_round_fp16(out, w0, W.step_seed(0))
+    got = out.view(torch.int16)
+    for a in (0, n // 2 - 777, n - (1 << 20)):
+        win = slice(a, a + (1 << 20))
+        assert_bit_equal(got[win].cpu().numpy().view(np.uint16),
+                         oracle.stochastic_round_fp16(to_np_f32(w0[win]), a, W.step_seed(0)), f"fp16 window {a}")
+    delta = (w0.abs() * f32(1e-4)).float()
+    fp32 = w0.clone()
+    sr = w0.to(torch.float16)
+    x = torch.empty_like(w0)
+    for t in range(1, 1001):
+        fp32 += delta
+        torch.add(sr.float(), delta, out=x)
+        mp.mp_stochastic_round_fp16(sr, x, W.step_seed(t))
+    rne = w0.to(torch.float16).float()
+    drift_sr = float((sr.float().double() / fp32.double() - 1.0).mean())
+    drift_rne = float((rne.double() / fp32.double() - 1.0).mean())
+    print(f"\nfp16 SR stress, 64M weights, 1000 steps: mean relative drift from the fp32 trajectory: "
+          f"stochastic rounding {drift_sr:+.3e}, round-to-nearest {drift_rne:+.3e}")
+    expect_rne = float(torch.where(w0 > 0, 1 / 1.1 - 1, 1 / 0.9 - 1).double().mean())
+    assert abs(drift_rne - expect_rne) < 1e-3
+    assert abs(drift_sr) < 1e-4, drift_sr
+
+
 # ---------------------------------------------------------------------------
 # gradient norm
 # ---------------------------------------------------------------------------
