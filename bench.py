@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import shutil
 import statistics
@@ -508,6 +509,32 @@ class OracleSample:
         assert st == 0
 
 
+def host_cpu() -> dict:
+    """The host's CPU model and core count, as the OS reports them."""
+    model = platform.processor() or platform.machine()
+    try:  # lscpu names Arm cores too (e.g. Neoverse-V2)
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, re.M)
+        if m:
+            return {"cpu_model": m.group(1).strip(), "nproc": os.cpu_count() or 1}
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+        m = re.search(r"^model name\s*:\s*(.+)$", text, re.M)
+        if m:
+            model = m.group(1).strip()
+        else:  # Arm hosts list an implementer and part number instead of a name
+            impl = re.search(r"^CPU implementer\s*:\s*(\S+)", text, re.M)
+            part = re.search(r"^CPU part\s*:\s*(\S+)", text, re.M)
+            if impl and part:
+                model = f"{platform.machine()} implementer {impl.group(1)} part {part.group(1)}"
+    except OSError:
+        pass
+    return {"cpu_model": model, "nproc": os.cpu_count() or 1}
+
+
 def cpu_baseline(seconds):
     """The oracle on a prefix of the set: single-threaded (the reported
     value), and on every host core (`all_cores`)."""
@@ -522,7 +549,7 @@ def cpu_baseline(seconds):
     dt = time.perf_counter() - t0
     out = {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": f"first {n} params of the GPT-2 124M set, {steps} steps (norm + AdamW + SR), "
-                     f"{dt:.1f} s, single-threaded C oracle"}
+                     f"{dt:.1f} s, single-threaded C oracle", **host_cpu()}
     out["all_cores"] = cpu_baseline_all_cores(seconds)
     return out
 
@@ -594,7 +621,8 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
                        "params": W.total(W.layout(W.specs_for(WORKLOAD))), "sample_params_per_step": n},
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                             **host_cpu()},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
