@@ -13,6 +13,8 @@
  *       "norm <value> scale <value> status <code>".
  *   mp_oracle_cli sr N IN OUT GLOBAL_OFFSET SEED
  *       OUT (bf16 patterns) = stochastic rounding of IN (fp32).
+ *   mp_oracle_cli sr16 N IN OUT GLOBAL_OFFSET SEED
+ *       OUT (fp16 patterns) = stochastic rounding of IN (fp32) to fp16.
  *   mp_oracle_cli noise FIRST N SEED
  *       Prints the N rounding draws from global index FIRST, one hex word per line.
  * Exit status 0 on success, 1 on a usage or I/O error, 2 if the step refused.
@@ -120,7 +122,7 @@ static int cmd_step(int argc, char** argv)
     return st != 0 ? 2 : (ok ? 0 : 1);
 }
 
-static int cmd_sr(int argc, char** argv)
+static int cmd_sr(int argc, char** argv, int to_fp16)
 {
     if (argc != 7)
         return 1;
@@ -129,7 +131,12 @@ static int cmd_sr(int argc, char** argv)
     uint16_t* out = malloc(n > 0 ? n * 2 : 1);
     if (!in || !out)
         return 1;
-    oracle_stochastic_round(out, in, strtoull(argv[5], NULL, 10), n, (uint32_t)strtoul(argv[6], NULL, 10));
+    const uint64_t goff = strtoull(argv[5], NULL, 10);
+    const uint32_t seed = (uint32_t)strtoul(argv[6], NULL, 10);
+    if (to_fp16)
+        oracle_stochastic_round_fp16(out, in, goff, n, seed);
+    else
+        oracle_stochastic_round(out, in, goff, n, seed);
     const int ok = write_file(argv[4], out, n * 2);
     free(in); free(out);
     return ok ? 0 : 1;
@@ -152,7 +159,9 @@ int main(int argc, char** argv)
     if (argc >= 2 && strcmp(argv[1], "step") == 0)
         rc = cmd_step(argc, argv);
     else if (argc >= 2 && strcmp(argv[1], "sr") == 0)
-        rc = cmd_sr(argc, argv);
+        rc = cmd_sr(argc, argv, 0);
+    else if (argc >= 2 && strcmp(argv[1], "sr16") == 0)
+        rc = cmd_sr(argc, argv, 1);
     else if (argc >= 2 && strcmp(argv[1], "noise") == 0)
         rc = cmd_noise(argc, argv);
     if (rc == 1)

@@ -69,13 +69,17 @@ def test_no_master_step_and_bad_table(tmp_path):
     assert r.returncode == 1
 
 
-def test_sr_and_noise_equal_the_library(tmp_path):
+def test_sr_sr16_and_noise_equal_the_library(tmp_path):
     rng = np.random.default_rng(2)
     x = (rng.standard_normal(5000) * 10.0 ** rng.uniform(-5, 5, 5000)).astype(np.float32)
     x.tofile(tmp_path / "x")
     r = _cli("sr", x.size, tmp_path / "x", tmp_path / "y", (1 << 32) - 77, 123)
     assert r.returncode == 0, r.stderr
     assert np.array_equal(np.fromfile(tmp_path / "y", np.uint16), oracle.stochastic_round(x, (1 << 32) - 77, 123))
+    r = _cli("sr16", x.size, tmp_path / "x", tmp_path / "h", (1 << 32) - 77, 123)
+    assert r.returncode == 0, r.stderr
+    assert np.array_equal(np.fromfile(tmp_path / "h", np.uint16),
+                          oracle.stochastic_round_fp16(x, (1 << 32) - 77, 123))
     r = _cli("noise", (1 << 32) - 2, 5, 9)
     assert r.returncode == 0
     got = [int(w, 16) for w in r.stdout.split()]
