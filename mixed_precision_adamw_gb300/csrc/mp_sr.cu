@@ -6,9 +6,12 @@
 // and §5.2 (bf16 weights are rebuilt from the fp32 master with the saved
 // rounding randomness, so a resumed run is bit-identical). Because the draw is
 // keyed on the global element index, the rebuild needs no launch-geometry
-// alignment: any grid gives the same bits. HBM-bound: 6 B per element. The
-// same section has the rounding write the encoder's embedding gradients: a
-// bf16 gradient plus an fp32 contribution, rounded back (8 B per element).
+// alignment: any grid gives the same bits. 6 B of HBM traffic per element;
+// at that ratio the draw's integer work (about 19 operations per element)
+// keeps the integer ALU pipe nearly saturated, so these kernels run a little
+// below the memory bound. The same section has the rounding write the
+// encoder's embedding gradients: a bf16 gradient plus an fp32 contribution,
+// rounded back (8 B per element).
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
