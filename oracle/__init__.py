@@ -54,6 +54,13 @@ def load_library(path: str) -> ctypes.CDLL:
     L.oracle_accumulate_sr.argtypes = [_c_u16p, _c_f32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
     L.oracle_sumsq.restype = ctypes.c_double
     L.oracle_sumsq.argtypes = [_c_u16p, ctypes.c_uint64]
+    L.oracle_sumsq_from.restype = ctypes.c_double
+    L.oracle_sumsq_from.argtypes = [ctypes.c_double, _c_u16p, ctypes.c_uint64]
+    L.oracle_norm_from_parts.restype = None
+    L.oracle_norm_from_parts.argtypes = [_c_f64p, ctypes.c_int32, ctypes.c_float, _c_f64p, _c_f32p, _c_f32p]
+    L.oracle_lr.restype = ctypes.c_float
+    L.oracle_lr.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, ctypes.c_float,
+                            ctypes.c_float, ctypes.c_int64]
     L.oracle_clip_scale.restype = ctypes.c_float
     L.oracle_clip_scale.argtypes = [ctypes.c_float, ctypes.c_float]
     L.oracle_grad_norm.restype = None
@@ -137,6 +144,31 @@ def accumulate_sr(acc: np.ndarray, delta: np.ndarray, global_offset: int, seed: 
 
 def sumsq(grads: np.ndarray) -> float:
     return float(lib().oracle_sumsq(_ptr(grads, _c_u16p, np.uint16), grads.size))
+
+
+def sumsq_from(s: float, grads: np.ndarray) -> float:
+    """s plus the squares of grads added one by one in index order."""
+    return float(lib().oracle_sumsq_from(s, _ptr(grads, _c_u16p, np.uint16), grads.size))
+
+
+def norm_from_parts(parts, clip: float):
+    """ZeRO-1 norm from per-rank sums of squares added in rank order.
+    Returns (sumsq: float64, norm: float32, scale: float32)."""
+    arr = np.ascontiguousarray(parts, dtype=np.float64)
+    s = ctypes.c_double()
+    nrm = ctypes.c_float()
+    sc = ctypes.c_float()
+    lib().oracle_norm_from_parts(_ptr(arr, _c_f64p, np.float64), arr.size, clip, ctypes.byref(s),
+                                 ctypes.byref(nrm), ctypes.byref(sc))
+    return s.value, np.float32(nrm.value), np.float32(sc.value)
+
+
+LR_CONSTANT, LR_COSINE, LR_LINEAR, LR_WSD = 0, 1, 2, 3
+
+
+def lr(kind: int, warmup: int, total: int, lr_max: float, lr_min: float, decay_frac: float, t: int) -> np.float32:
+    """Learning rate of the 1-based step t (NaN for invalid arguments)."""
+    return np.float32(lib().oracle_lr(kind, warmup, total, lr_max, lr_min, decay_frac, t))
 
 
 def clip_scale(norm: float, clip: float) -> float:

@@ -166,14 +166,18 @@ void oracle_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_off
 /* ---- Gradient norm ---------------------------------------------------------
  * [LLMC] §4: the global norm of all gradients, then the clip scale
  * min(1, 1.0 / grad_norm). The threshold 1.0 is an argument here. */
-double oracle_sumsq(const uint16_t* grads, uint64_t n)
+double oracle_sumsq_from(double s, const uint16_t* grads, uint64_t n)
 {
-    double s = 0.0;
     for (uint64_t i = 0; i < n; ++i) {
         const double g = (double)bf16_bits_to_float(grads[i]);
         s += g * g;
     }
     return s;
+}
+
+double oracle_sumsq(const uint16_t* grads, uint64_t n)
+{
+    return oracle_sumsq_from(0.0, grads, n);
 }
 
 float oracle_clip_scale(float norm, float clip)
@@ -195,6 +199,71 @@ void oracle_grad_norm(const uint16_t* grads, uint64_t n, float clip,
         *norm = nf;
     if (scale)
         *scale = oracle_clip_scale(nf, clip);
+}
+
+/* ---- ZeRO-1 norm --------------------------------------------------------
+ * [LLMC] §4: under ZeRO-1 each rank takes the sum of squares of its own
+ * shard only, and the per-rank sums are combined across ranks into the
+ * global norm. Reading taken here: the `count` per-rank sums are added in
+ * rank order, left to right, in fp64; the norm and clip scale then follow
+ * oracle_grad_norm. With one part this is oracle_grad_norm's result. */
+void oracle_norm_from_parts(const double* parts, int32_t count, float clip,
+                            double* sumsq, float* norm, float* scale)
+{
+    double s = 0.0;
+    for (int32_t r = 0; r < count; ++r)
+        s += parts[r];
+    const float root = (float)sqrt(s);
+    if (sumsq)
+        *sumsq = s;
+    if (norm)
+        *norm = root;
+    if (scale)
+        *scale = oracle_clip_scale(root, clip);
+}
+
+/* ---- Learning-rate schedules ----------------------------------------------
+ * [LLMC] §4 names four schedules (cosine, linear, constant, WSD) without
+ * formulas. Reading taken here, for the 1-based step t the update uses:
+ *   warm-up (t <= warmup): lr_max * t / warmup
+ *   afterwards, with p = (t - warmup) / (total - warmup) clamped to [0, 1]:
+ *     constant  lr_max
+ *     cosine    lr_min + (lr_max - lr_min) * (1 + cos(pi * p)) / 2
+ *     linear    lr_max - (lr_max - lr_min) * p
+ *     WSD       lr_max while p <= 1 - f (warm-up, stable), then linear from
+ *               lr_max to lr_min over the last fraction f of the steps:
+ *               lr_max - (lr_max - lr_min) * (p - (1 - f)) / f
+ * all in double, rounded to float once. Returns NaN for t < 1 or an invalid
+ * schedule (unknown kind, warmup < 0, total <= warmup for a decaying kind,
+ * f outside (0, 1] for WSD). */
+float oracle_lr(int32_t kind, int64_t warmup, int64_t total, float lr_max, float lr_min,
+                float decay_frac, int64_t t)
+{
+    if (t < 1 || warmup < 0 || kind < 0 || kind > 3)
+        return NAN;
+    if (kind != 0 && total <= warmup)
+        return NAN;
+    if (kind == 3 && !(decay_frac > 0.0f && decay_frac <= 1.0f))
+        return NAN;
+    const double hi = (double)lr_max, lo = (double)lr_min;
+    if (t <= warmup)
+        return (float)(hi * (double)t / (double)warmup);
+    if (kind == 0)
+        return lr_max;
+    double p = (double)(t - warmup) / (double)(total - warmup);
+    if (p > 1.0)
+        p = 1.0;
+    double lr;
+    if (kind == 1) {
+        const double pi = 3.14159265358979323846; /* the double nearest pi */
+        lr = lo + (hi - lo) * (1.0 + cos(pi * p)) / 2.0;
+    } else if (kind == 2) {
+        lr = hi - (hi - lo) * p;
+    } else {
+        const double f = (double)decay_frac;
+        lr = (p <= 1.0 - f) ? hi : hi - (hi - lo) * (p - (1.0 - f)) / f;
+    }
+    return (float)lr;
 }
 
 /* ---- Bias correction ----------------------------------------------------

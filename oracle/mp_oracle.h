@@ -66,7 +66,18 @@ void oracle_accumulate_sr(uint16_t* acc, const float* delta, uint64_t global_off
 
 /* Gradient norm: plain fp64 sum of squares in index order, then sqrt. */
 double oracle_sumsq(const uint16_t* grads, uint64_t n);
+/* The same sum continued from a running total s, in index order: summing a
+ * buffer in consecutive pieces gives exactly the one-pass sum. */
+double oracle_sumsq_from(double s, const uint16_t* grads, uint64_t n);
 float oracle_clip_scale(float norm, float clip);
+/* ZeRO-1: norm and clip scale from per-rank sums of squares added in rank
+ * order (fp64). */
+void oracle_norm_from_parts(const double* parts, int32_t count, float clip,
+                            double* sumsq, float* norm, float* scale);
+/* Learning rate of the 1-based step t: kind 0 constant, 1 cosine, 2 linear,
+ * 3 WSD, each after a linear warm-up; NaN for invalid arguments. */
+float oracle_lr(int32_t kind, int64_t warmup, int64_t total, float lr_max, float lr_min,
+                float decay_frac, int64_t t);
 void oracle_grad_norm(const uint16_t* grads, uint64_t n, float clip,
                       double* sumsq, float* norm, float* scale);
 

@@ -81,6 +81,28 @@ MUTANTS = {
          "const float sum = bf16_bits_to_float(acc[i]);"),
     "accumulate: draw keyed on the local index":
         ("acc[i] = oracle_sr(sum, global_offset + i, seed);", "acc[i] = oracle_sr(sum, i, seed);"),
+    "norm pieces: running total ignored":
+        ("double oracle_sumsq_from(double s, const uint16_t* grads, uint64_t n)\n{\n",
+         "double oracle_sumsq_from(double s, const uint16_t* grads, uint64_t n)\n{\n    s = 0.0;\n"),
+    "ZeRO-1 norm: parts added in reverse rank order":
+        ("    for (int32_t r = 0; r < count; ++r)\n        s += parts[r];",
+         "    for (int32_t r = count - 1; r >= 0; --r)\n        s += parts[r];"),
+    "ZeRO-1 norm: last part dropped":
+        ("    for (int32_t r = 0; r < count; ++r)\n        s += parts[r];",
+         "    for (int32_t r = 0; r + 1 < count; ++r)\n        s += parts[r];"),
+    "ZeRO-1 norm without the square root":
+        ("const float root = (float)sqrt(s);", "const float root = (float)s;"),
+    "lr: warm-up one step late":
+        ("return (float)(hi * (double)t / (double)warmup);", "return (float)(hi * (double)(t - 1) / (double)warmup);"),
+    "lr: cosine upside down":
+        ("lr = lo + (hi - lo) * (1.0 + cos(pi * p)) / 2.0;", "lr = lo + (hi - lo) * (1.0 - cos(pi * p)) / 2.0;"),
+    "lr: progress not clamped":
+        ("    if (p > 1.0)\n        p = 1.0;", "    if (p > 2.0)\n        p = 1.0;"),
+    "lr: WSD decays from the start of its last fraction's complement":
+        ("lr = (p <= 1.0 - f) ? hi : hi - (hi - lo) * (p - (1.0 - f)) / f;",
+         "lr = (p <= f) ? hi : hi - (hi - lo) * (p - f) / (1.0 - f);"),
+    "lr: linear decays to zero":
+        ("lr = hi - (hi - lo) * p;", "lr = hi - hi * p;"),
     "outlier: non-finite norms enter the window":
         ("    if (isfinite(x)) {\n        st->window", "    if (1) {\n        st->window"),
 }
@@ -124,6 +146,16 @@ def _pins():
         ("accumulate exact", P.test_accumulate_sr_exact_when_the_sum_is_representable),
         ("accumulate unbiased", P.test_accumulate_sr_is_unbiased_over_seeds),
         ("accumulate shards", P.test_accumulate_sr_keeps_small_contributions_and_shards),
+        ("norm in pieces", P.test_sumsq_continued_in_pieces_equals_one_pass),
+        ("ZeRO-1 norm exact", P.test_norm_from_parts_equals_whole_buffer_norm_on_exact_sums),
+        ("ZeRO-1 norm order", P.test_norm_from_parts_adds_in_rank_order_in_fp64),
+        ("ZeRO-1 norm bound", P.test_norm_from_parts_within_rounding_of_the_exact_sum),
+        ("lr warm-up", lambda: [P.test_lr_warmup_is_linear_and_reaches_the_peak(k) for k in range(4)]),
+        ("lr constant", P.test_lr_constant_after_warmup),
+        ("lr cosine", P.test_lr_cosine_closed_forms),
+        ("lr linear", P.test_lr_linear_closed_forms),
+        ("lr WSD", P.test_lr_wsd_closed_forms),
+        ("lr invalid", P.test_lr_rejects_invalid_arguments),
     ]
 
 

@@ -707,3 +707,151 @@ def test_outlier_window_ignores_nonfinite_norms_and_slides():
     assert z == math.inf and st == 8
     # the window now holds 127 ones and one 2.0 (the oldest slot was replaced)
     assert sorted(o.state.window)[-1] == 2.0 and sum(o.state.window) == 129.0
+
+
+# --------------------------------------------------------------------------
+# The norm in pieces — llm.c ch. 04 §4: the global norm covers every gradient;
+# under ZeRO-1 (§3.2, §4) each rank sums its own shard and the per-rank sums
+# are combined; CMU 11-667 lecture 13 notes §5.2: ZeRO-1 matches data
+# parallelism (max difference 0 on their example).
+# --------------------------------------------------------------------------
+def test_sumsq_continued_in_pieces_equals_one_pass():
+    rng = np.random.default_rng(5)
+    g = _bf16(rng.standard_normal(100_003) * 10.0 ** rng.uniform(-6, 3, 100_003))
+    whole = oracle.sumsq(g)
+    for cuts in ([0], [1], [50_000], [7, 64, 99_999], list(range(0, 100_003, 9_973))):
+        s, a = 0.0, 0
+        for c in cuts + [g.size]:
+            s = oracle.sumsq_from(s, g[a:c])
+            a = c
+        assert s == whole, cuts  # bit for bit: the same additions in the same order
+    # the running total is where the sum starts: 7 + 1000 * 1^2
+    ones = np.full(1000, 0x3F80, np.uint16)
+    assert oracle.sumsq_from(7.0, ones) == 1007.0
+    assert oracle.sumsq_from(2.5, ones[:0]) == 2.5
+
+
+def test_norm_from_parts_equals_whole_buffer_norm_on_exact_sums():
+    # +-2^k gradients: every sum of squares is exact in fp64, so 8 shard sums
+    # added in rank order give exactly the whole-buffer sum, norm and scale
+    rng = np.random.default_rng(9)
+    k = rng.integers(-8, 10, 8 * 4096)  # squares 2^-16 .. 2^18: 34 bits of range, 15 of count
+    g = _bf16(np.where(rng.random(k.size) < 0.5, -1.0, 1.0) * np.exp2(k.astype(np.float64)))
+    per = g.size // 8
+    parts = [oracle.sumsq(g[r * per:(r + 1) * per]) for r in range(8)]
+    s_w, n_w, sc_w = oracle.grad_norm(g, 1.0)
+    s_p, n_p, sc_p = oracle.norm_from_parts(parts, 1.0)
+    assert s_p == s_w == math.fsum(float(x) ** 2 for x in oracle.bf16_bits_to_f32(g).astype(np.float64))
+    assert n_p == n_w and sc_p == sc_w
+    # one part is oracle_grad_norm itself
+    assert oracle.norm_from_parts([s_w], 1.0) == (s_w, n_w, sc_w)
+
+
+def test_norm_from_parts_adds_in_rank_order_in_fp64():
+    # left to right: (2^53 + 1) rounds back to 2^53 (ties to even), and again
+    # for the next 1; another order would keep the two ones
+    s, nrm, sc = oracle.norm_from_parts([2.0 ** 53, 1.0, 1.0], 1.0)
+    assert s == 2.0 ** 53
+    s, _, _ = oracle.norm_from_parts([1.0, 1.0, 2.0 ** 53], 1.0)
+    assert s == 2.0 ** 53 + 2.0
+    # closed cases of the clip rule: sum 4 -> norm 2 -> scale 1/2; sum 0.25 -> 1
+    assert oracle.norm_from_parts([1.0, 3.0], 1.0)[1:] == (F32(2.0), F32(0.5))
+    assert oracle.norm_from_parts([0.25, 0.0], 1.0)[1:] == (F32(0.5), F32(1.0))
+    # a non-finite part refuses the step (NaN scale), like a non-finite norm
+    assert math.isnan(oracle.norm_from_parts([1.0, math.inf], 1.0)[2])
+    assert math.isnan(oracle.norm_from_parts([math.nan], 1.0)[2])
+
+
+def test_norm_from_parts_within_rounding_of_the_exact_sum():
+    rng = np.random.default_rng(12)
+    g = _bf16(rng.standard_normal(80_000) * 1e-3)
+    exact = math.fsum(float(x) ** 2 for x in oracle.bf16_bits_to_f32(g).astype(np.float64))
+    for world in (2, 4, 8):
+        per = g.size // world
+        parts = [oracle.sumsq(g[r * per:(r + 1) * per]) for r in range(world)]
+        s, _, _ = oracle.norm_from_parts(parts, 1.0)
+        assert abs(s - exact) <= g.size * 2.0 ** -53 * exact
+
+
+# --------------------------------------------------------------------------
+# Learning-rate schedules — llm.c ch. 04 §4 names four (cosine, linear,
+# constant, WSD) without formulas; the reading is in the oracle's comment.
+# Pinned by closed forms at chosen steps and by the shapes' invariants.
+# --------------------------------------------------------------------------
+def _ulp_close(a, b, ulps=1):
+    a, b = F32(a), F32(b)
+    return abs(int(a.view(np.int32)) - int(b.view(np.int32))) <= ulps
+
+
+LR = dict(warmup=10, total=110, lr_max=6e-4, lr_min=6e-5)
+
+
+def _lr(kind, t, **kw):
+    a = {**LR, **kw}
+    return oracle.lr(kind, a["warmup"], a["total"], a["lr_max"], a["lr_min"], a.get("decay_frac", 0.2), t)
+
+
+@pytest.mark.parametrize("kind", [oracle.LR_CONSTANT, oracle.LR_COSINE, oracle.LR_LINEAR, oracle.LR_WSD])
+def test_lr_warmup_is_linear_and_reaches_the_peak(kind):
+    hi = F32(LR["lr_max"])
+    assert _lr(kind, 10) == hi  # the last warm-up step reaches lr_max exactly
+    assert _lr(kind, 5) == F32(float(hi) / 2)  # half way: exactly half (a power-of-two ratio)
+    assert _ulp_close(_lr(kind, 1), float(hi) / 10)
+    ramp = [float(_lr(kind, t)) for t in range(1, 11)]
+    assert all(b > a for a, b in zip(ramp, ramp[1:]))
+    # no warm-up: the first step is already past it
+    assert _lr(kind, 1, warmup=0) <= hi
+
+
+def test_lr_constant_after_warmup():
+    for t in (11, 50, 110, 10_000):
+        assert _lr(oracle.LR_CONSTANT, t) == F32(LR["lr_max"])
+
+
+def test_lr_cosine_closed_forms():
+    hi, lo = float(F32(LR["lr_max"])), float(F32(LR["lr_min"]))
+    assert _ulp_close(_lr(oracle.LR_COSINE, 60), (hi + lo) / 2)  # p = 1/2: cos = 0
+    assert _ulp_close(_lr(oracle.LR_COSINE, 35), lo + (hi - lo) * (1 + math.sqrt(0.5)) / 2)  # p = 1/4
+    assert _ulp_close(_lr(oracle.LR_COSINE, 85), lo + (hi - lo) * (1 - math.sqrt(0.5)) / 2)  # p = 3/4
+    assert _lr(oracle.LR_COSINE, 110) == F32(lo)  # p = 1: cos = -1
+    assert _lr(oracle.LR_COSINE, 500) == F32(lo)  # past the end: stays at lr_min
+    # symmetric about the middle: lr(mid - d) + lr(mid + d) = hi + lo
+    for d in (1, 7, 33, 49):
+        s = float(_lr(oracle.LR_COSINE, 60 - d)) + float(_lr(oracle.LR_COSINE, 60 + d))
+        assert abs(s - (hi + lo)) <= 2 * 2.0 ** -24 * hi
+    tail = [float(_lr(oracle.LR_COSINE, t)) for t in range(10, 111)]
+    assert all(b <= a for a, b in zip(tail, tail[1:]))
+
+
+def test_lr_linear_closed_forms():
+    hi, lo = float(F32(LR["lr_max"])), float(F32(LR["lr_min"]))
+    assert _ulp_close(_lr(oracle.LR_LINEAR, 35), hi - (hi - lo) / 4)
+    assert _ulp_close(_lr(oracle.LR_LINEAR, 60), (hi + lo) / 2)
+    assert _lr(oracle.LR_LINEAR, 110) == F32(lo)
+    assert _lr(oracle.LR_LINEAR, 111) == F32(lo)
+    # equal steps down: constant differences
+    d = [float(_lr(oracle.LR_LINEAR, t)) - float(_lr(oracle.LR_LINEAR, t + 1)) for t in range(11, 109)]
+    assert max(d) - min(d) <= 4 * 2.0 ** -24 * hi
+
+
+def test_lr_wsd_closed_forms():
+    hi, lo = float(F32(LR["lr_max"])), float(F32(LR["lr_min"]))
+    # stable at lr_max for the first 80 % of the post-warm-up steps
+    for t in range(11, 91):
+        assert _lr(oracle.LR_WSD, t) == F32(hi), t
+    assert _ulp_close(_lr(oracle.LR_WSD, 100), (hi + lo) / 2)  # half way through the decay
+    assert _ulp_close(_lr(oracle.LR_WSD, 95), hi - (hi - lo) / 4)
+    assert _lr(oracle.LR_WSD, 110) == F32(lo)
+    # decay over the whole run (f = 1) is the linear schedule
+    for t in range(11, 111):
+        assert _ulp_close(_lr(oracle.LR_WSD, t, decay_frac=1.0), _lr(oracle.LR_LINEAR, t)), t
+
+
+def test_lr_rejects_invalid_arguments():
+    assert math.isnan(_lr(oracle.LR_COSINE, 0))
+    assert math.isnan(_lr(oracle.LR_COSINE, 5, total=10))  # total <= warmup for a decaying kind
+    assert math.isnan(_lr(oracle.LR_WSD, 20, decay_frac=0.0))
+    assert math.isnan(_lr(oracle.LR_WSD, 20, decay_frac=1.5))
+    assert math.isnan(oracle.lr(4, 0, 10, 1e-3, 0.0, 0.5, 3))
+    assert math.isnan(oracle.lr(oracle.LR_LINEAR, -1, 10, 1e-3, 0.0, 0.5, 3))
+    assert _lr(oracle.LR_CONSTANT, 5, total=0) == F32(LR["lr_max"] / 2)  # constant ignores total
