@@ -1,24 +1,30 @@
 """Benchmark of the mixed-precision optimizer step on GB300.
 
-One step = the whole hot path over the GPT-2 124M parameter set (124,475,904
-params, 148 tensors, one flat buffer): global grad norm + clip scale
-(mp_grad_norm: two kernels) and the fused AdamW + stochastic-rounding step
-with fp32 master weights (mp_adamw_step: one kernel). Inputs are synthetic and
-already resident in HBM; the 3.5 GB of state touched per step is far larger
-than the 129 MB L2, so no flush is needed between steps.
+One step = the whole hot path over the Llama-3-8B parameter set (8,030,261,248
+params, 291 tensors, one flat buffer, about 128 GB of optimizer state in HBM):
+global grad norm + clip scale (mp_grad_norm: two kernels) and the fused
+AdamW + stochastic-rounding step with fp32 master weights (mp_adamw_step: 40
+launches of about 200M elements). Inputs are synthetic and already resident in
+HBM; the 241 GB touched per step are far larger than the 129 MB L2, so no
+flush is needed between steps.
 
 Prints ONE JSON line (rank 0). Also reports: the roofline of the dominant
-kernel (the step kernel, 28 algorithmic bytes per parameter) against the
-measured HBM copy bandwidth, the other path variants (no-master step, norm,
-standalone rounding, 8 ZeRO-1 shard launches), an end-to-end number through
-the C ABI with the gradients copied from pinned host memory every step, SM
-clocks sampled during the timed region, and the CPU oracle timed on a bounded
-sample as a reported baseline.
+kernel (the step kernel, 28 algorithmic bytes per parameter, timed over 16 or
+more event-bracketed steps after the timed region) against the measured HBM
+copy bandwidth, with its DRAM traffic scaled from a committed ncu capture;
+the other path variants (no-master step, norm, standalone roundings, 8 ZeRO-1
+shard launches; the GPT-2 1.5B set whole and as 8 shards; the
+stochastic-rounding stress set: kernel throughput and 1000-step drift); an
+end-to-end number through the C ABI with the gradients copied from pinned
+host memory every step; SM clocks sampled during the timed region; and the
+CPU oracle timed on a bounded sample as a reported baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-With N > 1 (launched by torch.distributed.run) every rank runs an independent
-replica of the step on its own GPU (weak scaling, no data-path collective);
-the time is the max over ranks.
+                  [--workload tiny|gpt2_124m|gpt2_1558m|llama3_8b]
+With N > 1 (launched by torch.distributed.run) the ranks run the ZeRO-1 step
+(zero1.py): reduce-scatter of the gradients, each rank's shard of the norm and
+the update, all-gather of the bf16 weights; the time is the max over ranks.
+--replicas runs an independent single-GPU step per rank instead.
 """
 import argparse
 import hashlib
@@ -43,7 +49,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "AdamW+SR step: Gparams/s and HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "Gparams/s"
-WORKLOAD = "gpt2_124m"  # the default line; --workload picks the other parameter sets
+WORKLOAD = "llama3_8b"  # the default line; --workload picks the other parameter sets
 WORKLOAD_NAMES = {
     "tiny": "tiny GPT-style parameter set (d 32, 2 layers, 28,672 params)",
     "gpt2_124m": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
@@ -60,9 +66,8 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only)
 STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
                        "mixed_precision_adamw_gb300/csrc/mp_step.cuh",
                        "mixed_precision_adamw_gb300/csrc/mp_device.cuh"]
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_gpt2_124m.md")
-SAMPLE_EVERY = 8
-GRAPH_STEPS = 20
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_traffic.json")
+KERNEL_SAMPLES = 16  # event-bracketed step calls after the timed region, at least
 
 
 # ---------------------------------------------------------------------------
@@ -126,18 +131,21 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic_bytes():
-    """DRAM bytes per launch of the step kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def profiled_traffic_bytes(launch_elems: float):
+    """DRAM bytes (read + write) of one step-kernel launch of `launch_elems`
+    elements, from the committed ncu capture whose launch size is closest,
+    scaled by elements (the kernel streams each element once), if that
+    capture was taken on the current kernel source; else None."""
     try:
-        text = open(TRAFFIC_PROFILE).read()
-    except OSError:
-        return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
-        return None
-    return int(float(m.group(1)))
+        with open(TRAFFIC_PROFILE) as f:
+            prof = json.load(f)
+    except (OSError, ValueError):
+        return None, None
+    if prof.get("kernel_source_sha256_16") != kernel_source_hash() or not prof.get("captures"):
+        return None, None
+    cap = min(prof["captures"], key=lambda c: abs(c["launch_elems"] - launch_elems))
+    per_elem = (cap["dram_bytes_read"] + cap["dram_bytes_write"]) / cap["launch_elems"]
+    return int(round(per_elem * launch_elems)), cap["launch_elems"]
 
 
 class ClockSampler:
@@ -232,40 +240,57 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
 
-    # Events bracket the step kernel on every SAMPLE_EVERY-th step only: an
-    # event between two kernels stops the next one from being scheduled early
-    # (programmatic dependent launch), so bracketing every step would slow the
-    # timed loop it measures.
-    sample = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for i in range(0, args.steps, SAMPLE_EVERY)}
+    # The timed region: K chained steps (the kernels of consecutive steps
+    # follow each other with programmatic dependent launch; no event sits
+    # between them).
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     torch.cuda.synchronize()
     barrier(world)
     start.record(stream)
-    for i in range(args.steps):
-        one_step(sample.get(i))
+    for _ in range(args.steps):
+        one_step()
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
     total_ms = start.elapsed_time(end)
-    step_kernel_times = [a.elapsed_time(b) for a, b in sample.values()]
-    step_kernel_ms = statistics.mean(step_kernel_times)
     opt.check_status()
     max_s = max_over_ranks(total_ms / 1e3, world, device)
     value = whole_job_value(N, world, args.steps, max_s)
     ms_per_step = max_s * 1e3 / args.steps
 
+    # The step kernel alone: events around the update of each of
+    # KERNEL_SAMPLES further steps (norm, event, update, event), so the
+    # sample count does not depend on --steps. A step's update is one or more
+    # launches of the same kernel (ranges above 201,326,592 elements are cut
+    # into near-equal launches); the events bracket all of them.
+    launches = len(mp.mp_step_launches(0, N, opt.table))
+    samples = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(KERNEL_SAMPLES, args.kernel_samples))]
+    for ev in samples:
+        one_step(ev)
+    torch.cuda.synchronize()
+    opt.check_status()
+    step_call_ms = [a.elapsed_time(b) for a, b in samples]
+    step_kernel_ms = statistics.mean(step_call_ms)
+
     peak, peak_kind = measured_hbm_peak()
     achieved = STEP_BYTES_MASTER * N / (step_kernel_ms / 1e3) / 1e9
-    traffic = profiled_traffic_bytes() if workload == WORKLOAD else None
+    traffic, traffic_from = profiled_traffic_bytes(N / launches) if not args.params else (None, None)
     roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master>", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                "traffic": traffic, "algorithmic_bytes_per_launch": STEP_BYTES_MASTER * N,
-                "kernel_ms": round(step_kernel_ms, 5), "kernel_ms_samples": len(sample),
-                "kernel_ms_median": round(statistics.median(step_kernel_times), 5),
-                "kernel_ms_min": round(min(step_kernel_times), 5)}
+                "traffic": traffic,
+                "traffic_source": (f"ncu capture of a {traffic_from}-element launch (profiles/adamw_step_traffic.json), "
+                                   f"scaled by elements to this workload's launches" if traffic else None),
+                "algorithmic_bytes_per_launch": round(STEP_BYTES_MASTER * N / launches),
+                "launches_per_step": launches,
+                "kernel_ms_per_launch": round(step_kernel_ms / launches, 5),
+                "kernel_ms_per_step": round(step_kernel_ms, 5), "kernel_ms_samples": len(samples),
+                "kernel_ms_per_step_median": round(statistics.median(step_call_ms), 5),
+                "kernel_ms_per_step_min": round(min(step_call_ms), 5),
+                "how": "achieved = 28 B x params / mean CUDA-event time of a step's update launches "
+                       "(= algorithmic bytes per launch / mean launch duration)"}
 
     roofline["frac_of_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
     if args.quick:
@@ -280,7 +305,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return None
     # norm partials + norm finalize + the step's launches, as the library splits them
-    launches_per_step = 2 + len(mp.mp_step_launches(0, N, opt.table))
+    launches_per_step = 2 + launches
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -300,10 +325,146 @@ def run_ours(args, world, rank, local):
     }
     if args.params:
         line["config"]["workload"] += f", first {N} params only"
-        line["roofline"]["traffic"] = None
+    if not args.quick:
+        # other parameter sets, after this one's state is released
+        del st, grads, opt
+        torch.cuda.empty_cache()
+        if workload == WORKLOAD and not args.params:
+            line["variants"]["gpt2_1558m_whole_vs_8_shards"] = measure_shards_1558m(mp, stream, device, peak)
+        line["variants"]["sr_stress"] = measure_sr_stress(mp, stream, device, peak)
     if world == 1 and not args.no_cpu_baseline and not args.quick:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, workload)
     return line
+
+
+def run_zero1(args, world, rank, local):
+    """The ZeRO-1 step over `world` ranks (llm.c ch. 04 §3.2-§3.3, §4):
+    reduce-scatter of the gradients, the shard's share of the norm,
+    all-gather of the per-rank sums, the shard update, all-gather of the
+    bf16 weights. The whole model's parameters are updated once per step
+    across all ranks, so the value is params x steps / the slowest rank's
+    time (strong scaling: the work per step does not grow with N)."""
+    import mixed_precision_adamw_gb300 as mp
+    from mixed_precision_adamw_gb300.zero1 import Zero1Optimizer
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if not torch.distributed.is_initialized():
+        if world == 1:  # a one-rank group outside torchrun (--zero1)
+            import socket
+            with socket.socket() as sk:
+                sk.bind(("127.0.0.1", 0))
+                port = sk.getsockname()[1]
+            for k, v in (("MASTER_ADDR", "127.0.0.1"), ("MASTER_PORT", str(port)), ("RANK", "0"),
+                         ("WORLD_SIZE", "1")):
+                os.environ.setdefault(k, v)
+        torch.distributed.init_process_group(backend="nccl")
+    H = W.HYPER
+    workload = args.workload
+    entries = W.layout(W.specs_for(workload))
+    if args.params:
+        entries = prefix_entries(entries, args.params)
+    tab = W.table(entries)
+    N = W.total(entries)
+    zopt = Zero1Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                          weight_decay=H["weight_decay"], clip=H["clip"], device=device)
+    per = zopt.layout.size
+    st = W.make_state(workload, device=device, entries=entries)
+    params = st["params"]
+    shard = zopt.make_shard_state(st["master"])
+    del st
+    torch.cuda.empty_cache()
+    # each rank's backward pass gives its own gradients: seeded by rank
+    grads = [W.make_grads(workload, s, device=device, entries=entries, seed=W.BASE_SEED + 7919 * rank)
+             for s in (1, 2)]
+    stream = torch.cuda.current_stream(device)
+    step_no = [0]
+
+    def one_step(g=None):
+        step_no[0] += 1
+        t = step_no[0]
+        zopt.step(params, grads[t % 2] if g is None else g, shard["master"], shard["m"], shard["v"], t,
+                  W.step_seed(t), stream=stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    start.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    assert zopt.take_status() == 0
+    max_s = max_over_ranks(total_ms / 1e3, world, device)
+    value = N * args.steps / max_s / 1e9
+    ms_per_step = max_s * 1e3 / args.steps
+
+    # the shard update alone (the dominant kernel), after the timed region
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
+    sl = zopt.layout.slice()
+    ms = time_events(lambda: mp.mp_adamw_step(params[sl], zopt.grad_shard, shard["master"], shard["m"],
+                                              shard["v"], zopt.table, d_grad_scale=zopt.d_scale, t=step_no[0],
+                                              seed=1, global_offset=zopt.layout.offset, n=per, stream=stream, **kw),
+                     max(KERNEL_SAMPLES, args.kernel_samples), stream)
+    launches = len(mp.mp_step_launches(zopt.layout.offset, per, zopt.table))
+    peak, peak_kind = measured_hbm_peak()
+    achieved = STEP_BYTES_MASTER * per / ms / 1e6
+    traffic, traffic_from = profiled_traffic_bytes(per / launches) if not args.params else (None, None)
+    roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master> (this rank's shard)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": round(STEP_BYTES_MASTER * per / launches),
+                "launches_per_step": launches, "kernel_ms_per_step": round(ms, 5),
+                "kernel_ms_samples": LAST_TIMING["launches"]}
+    e2e = None
+    if not args.quick:
+        # end to end: this rank's gradients from pinned host memory, the
+        # norm read back every step
+        host_g = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
+        host_g.copy_(grads[0])
+        dev_g = grads[1]
+        host_norm = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        iters = min(args.steps, 50)
+
+        def e2e_step():
+            dev_g.copy_(host_g, non_blocking=True)
+            one_step(dev_g)
+            host_norm.copy_(zopt.d_norm, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_s = max_over_ranks(a.elapsed_time(b) / 1e3, world, device)
+        e2e = {"value": round(N * iters / e_s / 1e9, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * N,
+               "d2h_bytes_per_step": 4, "steps": iters,
+               "api": "Zero1Optimizer.step (per rank: gradients copied from pinned host memory first)"}
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[workload] + (f", first {N} params only" if args.params else ""),
+                   "params": N, "shard_params": per, "tensors": len(entries),
+                   "variant": "fp32 master + bf16 params, clip 1.0",
+                   "l2": f"no flush: {30 * per / 1e9:.2f} GB of optimizer traffic per rank per step, > 129 MB L2",
+                   "parallelism": f"zero1 dp{world} (NCCL reduce-scatter avg, all-gather)"},
+        "roofline": roofline, "e2e": e2e, "clocks": clocks,
+        # per step: norm partials + sums-only finalize + scale + the shard's launches
+        "gpu_launches": (3 + launches) * args.steps,
+    }
 
 
 LAST_TIMING = {}
@@ -377,48 +538,6 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     out["accumulate_sr"] = {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(N / ms / 1e6, 2),
                             "gbs": round(ACC_BYTES * N / ms / 1e6, 1),
                             "frac": round(ACC_BYTES * N / ms / 1e6 / peak, 4), "bytes_per_elem": ACC_BYTES}
-    # Steps as CUDA graphs. "graph_step": one graph holding GRAPH_STEPS
-    # consecutive mp_optimizer_step_graph calls (the step count lives on the
-    # device, so each captured call is the next step), replayed back to back:
-    # the device time per step without per-launch host work.
-    # "graph_separate_kernels": the same with the separate calls (norm,
-    # finalize and update kernels: the general path) captured instead.
-    opt.init_device_clock(t=1000, seed_base=W.BASE_SEED)
-    opt.step_graph(st["params"], g, st["master"], st["m"], st["v"], stream=stream)
-    torch.cuda.synchronize()
-
-    def graph_ms(one_step):
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for _ in range(GRAPH_STEPS):
-                one_step()
-        reps = max(2, min(50, int(2e9 / max(1, 30 * N * GRAPH_STEPS))))
-        graph.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        del graph
-        return a.elapsed_time(b) / (reps * GRAPH_STEPS), reps
-
-    ms, reps = graph_ms(lambda: opt.step_graph(st["params"], g, st["master"], st["m"], st["v"]))
-    opt.check_status()
-    out["graph_step"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
-                         "gbs": round((STEP_BYTES_MASTER + NORM_BYTES) * N / ms / 1e6, 1),
-                         "steps_per_graph": GRAPH_STEPS, "replays": reps,
-                         "what": "mp_optimizer_step_graph captured in a CUDA graph, replayed back to back"}
-
-    def separate():
-        mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N)
-        mp.mp_adamw_step(st["params"], g, st["master"], st["m"], st["v"], opt.table, d_grad_scale=opt.d_scale,
-                         t=7, seed=7, n=N, **kw)
-    ms, reps = graph_ms(separate)
-    out["graph_separate_kernels"] = {"ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
-                                     "steps_per_graph": GRAPH_STEPS, "replays": reps,
-                                     "what": "mp_grad_norm + mp_adamw_step (3 kernels) captured the same way"}
     per = N // 8
 
     def shards():
@@ -433,13 +552,92 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     return out
 
 
+def measure_shards_1558m(mp, stream, device, peak):
+    """The GPT-2 1.5B set (1,557,686,400 params): one whole-buffer step
+    against the same step as 8 contiguous shard launches of 194,710,800
+    params each (the ZeRO-1 layout on one GPU, no communication). The tests
+    check that both give the same bits."""
+    H = W.HYPER
+    name = "gpt2_1558m"
+    entries = W.layout(W.specs_for(name))
+    tab = W.table(entries)
+    N = W.total(entries)
+    st = W.make_state(name, device=device)
+    g = W.make_grads(name, 1, device=device)
+    opt = mp.Optimizer(tab, lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"],
+                       weight_decay=H["weight_decay"], clip=H["clip"], device=device)
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"],
+              d_grad_scale=opt.d_scale, stream=stream)
+    mp.mp_grad_norm(g, H["clip"], opt.workspace, opt.d_norm, opt.d_scale, n=N, stream=stream)
+    per = N // 8
+    ms_whole = time_events(lambda: mp.mp_adamw_step(st["params"], g, st["master"], st["m"], st["v"], opt.table,
+                                                    t=1, seed=W.step_seed(1), n=N, **kw), 10, stream)
+    whole = dict(LAST_TIMING)
+
+    def shards():
+        for r in range(8):
+            sl = slice(r * per, (r + 1) * per)
+            mp.mp_adamw_step(st["params"][sl], g[sl], st["master"][sl], st["m"][sl], st["v"][sl], opt.table,
+                             t=1, seed=W.step_seed(1), global_offset=r * per, n=per, **kw)
+    ms_sh = time_events(shards, 10, stream)
+    out = {"params": N, "shard_params": per,
+           "whole": {**whole, "ms": round(ms_whole, 5), "gparams_s": round(N / ms_whole / 1e6, 2),
+                     "gbs": round(STEP_BYTES_MASTER * N / ms_whole / 1e6, 1),
+                     "frac": round(STEP_BYTES_MASTER * N / ms_whole / 1e6 / peak, 4),
+                     "launches": len(mp.mp_step_launches(0, N, opt.table))},
+           "shards_8": {**LAST_TIMING, "ms": round(ms_sh, 5), "gparams_s": round(N / ms_sh / 1e6, 2),
+                        "gbs": round(STEP_BYTES_MASTER * N / ms_sh / 1e6, 1),
+                        "frac": round(STEP_BYTES_MASTER * N / ms_sh / 1e6 / peak, 4),
+                        "launches": sum(len(mp.mp_step_launches(r * per, per, opt.table)) for r in range(8))},
+           "what": "mp_adamw_step with fp32 master over the whole buffer vs 8 shard calls (global offsets r*N/8)"}
+    del st, g, opt
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_sr_stress(mp, stream, device, peak, n=64 << 20, steps=1000):
+    """The stochastic-rounding stress set: 64M fp32 weights, |w| log-uniform
+    in [1e-3, 10], random sign. (1) Throughput of the standalone rounding
+    kernel on it (6 B per element). (2) A constant update of 1e-4 |w| per
+    element (below half a bf16 step) for 1000 steps: the mean relative drift
+    of the bf16 weights from the fp32 trajectory with stochastic rounding
+    (mp_accumulate_sr: w = SR((float)w + delta), one kernel per step) and with
+    round-to-nearest (the bf16 cast of (float)w + delta)."""
+    w0 = W.sr_stress_weights(n, device=device)
+    out16 = torch.empty(n, dtype=torch.bfloat16, device=device)
+    ms = time_events(lambda: mp.mp_stochastic_round(out16, w0, 7, stream=stream), 20, stream)
+    res = {"elements": n, "sr_kernel": {**LAST_TIMING, "ms": round(ms, 5), "gelems_s": round(n / ms / 1e6, 2),
+                                        "gbs": round(SR_BYTES * n / ms / 1e6, 1),
+                                        "frac": round(SR_BYTES * n / ms / 1e6 / peak, 4),
+                                        "bytes_per_elem": SR_BYTES}}
+    delta = (w0.abs() * 1e-4).float()
+    fp32 = w0.clone()
+    sr = w0.to(torch.bfloat16)
+    rne = w0.to(torch.bfloat16)
+    tmp = torch.empty_like(w0)
+    for t in range(1, steps + 1):
+        fp32 += delta
+        mp.mp_accumulate_sr(sr, delta, W.step_seed(t), stream=stream)
+        torch.add(rne.float(), delta, out=tmp)
+        rne.copy_(tmp)  # the round-to-nearest cast
+    torch.cuda.synchronize()
+    ref = fp32.double()
+    res["drift"] = {"steps": steps, "update": "1e-4 |w0| per step",
+                    "sr_mean_rel": float((sr.double() / ref - 1.0).mean()),
+                    "rne_mean_rel": float((rne.double() / ref - 1.0).mean()),
+                    "what": "mean over elements of bf16 weight / fp32 trajectory - 1 after the last step"}
+    del w0, out16, delta, fp32, sr, rne, tmp
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_e2e(mp, st, g, opt, N, stream, device, kw, iters, step_no):
     """Through the public API with host buffers: every step is one
     mp_optimizer_step call that takes the bf16 gradients from pinned host
     memory (the norm kernel reads them over the host link and writes the
     device copy), and the norm and status are read back to the host."""
     host_g = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
-    host_g.copy_(g.cpu())
+    host_g.copy_(g)
     dev_g = torch.empty_like(g)
     host_norm = torch.empty(1, dtype=torch.float32, pin_memory=True)
     host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
@@ -484,17 +682,17 @@ def prefix_entries(entries, n):
 class OracleSample:
     """The first `n` params of the workload on the host, stepped by the oracle."""
 
-    def __init__(self, n):
+    def __init__(self, n, workload=WORKLOAD):
         import oracle
         self.oracle = oracle
-        entries = prefix_entries(W.layout(W.specs_for(WORKLOAD)), n)
+        entries = prefix_entries(W.layout(W.specs_for(workload)), n)
         self.tab = W.table(entries)
-        st = W.make_state(WORKLOAD, entries=entries)
+        st = W.make_state(workload, entries=entries)
         self.params = W.bf16_bits(st["params"]).copy()
         self.master = st["master"].numpy().copy()
         self.m = st["m"].numpy().copy()
         self.v = st["v"].numpy().copy()
-        self.grads = [W.bf16_bits(W.make_grads(WORKLOAD, s, entries=entries)).copy() for s in (1, 2)]
+        self.grads = [W.bf16_bits(W.make_grads(workload, s, entries=entries)).copy() for s in (1, 2)]
         self.n = n
         self.t = 0
 
@@ -535,11 +733,11 @@ def host_cpu() -> dict:
     return {"cpu_model": model, "nproc": os.cpu_count() or 1}
 
 
-def cpu_baseline(seconds):
+def cpu_baseline(seconds, workload=WORKLOAD):
     """The oracle on a prefix of the set: single-threaded (the reported
     value), and on every host core (`all_cores`)."""
     n = 1 << 22
-    s = OracleSample(n)
+    s = OracleSample(n, workload)
     s.step()
     t0 = time.perf_counter()
     steps = 0
@@ -548,13 +746,13 @@ def cpu_baseline(seconds):
         steps += 1
     dt = time.perf_counter() - t0
     out = {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
-           "sample": f"first {n} params of the GPT-2 124M set, {steps} steps (norm + AdamW + SR), "
+           "sample": f"first {n} params of the {WORKLOAD_NAMES[workload]}, {steps} steps (norm + AdamW + SR), "
                      f"{dt:.1f} s, single-threaded C oracle", **host_cpu()}
-    out["all_cores"] = cpu_baseline_all_cores(seconds)
+    out["all_cores"] = cpu_baseline_all_cores(seconds, workload)
     return out
 
 
-def cpu_baseline_all_cores(seconds, n=1 << 24):
+def cpu_baseline_all_cores(seconds, workload=WORKLOAD, n=1 << 24):
     """The same oracle on every host core: the norm as it stands (one thread,
     one sequential sum), then the step over contiguous shards, one thread
     each. Sharding the step changes no result (every element is independent
@@ -562,7 +760,7 @@ def cpu_baseline_all_cores(seconds, n=1 << 24):
     parallel."""
     import threading
     cores = os.cpu_count() or 1
-    s = OracleSample(n)
+    s = OracleSample(n, workload)
     per = ((n + cores - 1) // cores + 7) // 8 * 8
     bounds = [(a, min(n, a + per)) for a in range(0, n, per)]
     H = W.HYPER
@@ -592,22 +790,24 @@ def cpu_baseline_all_cores(seconds, n=1 << 24):
         steps += 1
     dt = time.perf_counter() - t0
     return {"value": round(n * steps / dt / 1e9, 5), "unit": UNIT, "cores": len(bounds), "kind": "oracle",
-            "sample": f"first {n} params of the GPT-2 124M set, {steps} steps, {dt:.1f} s: norm on one thread, "
+            "sample": f"first {n} params of the {WORKLOAD_NAMES[workload]}, {steps} steps, {dt:.1f} s: "
+                      f"norm on one thread, "
                       f"step on {len(bounds)} threads over contiguous shards"}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
+    workload = args.workload
     budget = args.cpu_seconds if args.cpu_seconds else 30.0
-    probe = OracleSample(1 << 18)
+    probe = OracleSample(1 << 18, workload)
     t0 = time.perf_counter()
     probe.step()
     per_param = (time.perf_counter() - t0) / probe.n
     total_steps = args.steps + args.warmup
     n = int(budget / max(1, total_steps) / per_param)
     n = max(1 << 12, min(n, 1 << 24)) & ~7
-    s = OracleSample(n)
+    s = OracleSample(n, workload)
     for _ in range(args.warmup):
         s.step()
     t0 = time.perf_counter()
@@ -615,12 +815,13 @@ def run_reference(args, world, rank):
         s.step()
     dt = time.perf_counter() - t0
     value = n * args.steps / dt / 1e9
-    sample = f"first {n} params of the GPT-2 124M set per step (norm + AdamW + SR), single-threaded C oracle"
+    sample = (f"first {n} params of the {WORKLOAD_NAMES[workload]} per step (norm + AdamW + SR), "
+              f"single-threaded C oracle")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "GPT-2 124M parameter set (V 50304, T 1024, d 768, 12 layers, tied wte)",
-                       "params": W.total(W.layout(W.specs_for(WORKLOAD))), "sample_params_per_step": n},
+            "config": {"workload": WORKLOAD_NAMES[workload],
+                       "params": W.total(W.layout(W.specs_for(workload))), "sample_params_per_step": n},
             "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
                              **host_cpu()},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -629,15 +830,21 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_NAMES), default=WORKLOAD,
-                    help="parameter set (default: the GPT-2 124M line)")
+                    help="parameter set (default: the Llama-3-8B line)")
     ap.add_argument("--params", type=int, default=0,
                     help="use only the first P params of the set (small cases for profiling)")
+    ap.add_argument("--kernel-samples", type=int, default=KERNEL_SAMPLES,
+                    help="event-bracketed step calls after the timed region (at least 16)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="with N > 1: an independent single-GPU step per rank instead of ZeRO-1")
+    ap.add_argument("--zero1", action="store_true",
+                    help="run the ZeRO-1 step even on one rank (a one-rank NCCL group)")
     ap.add_argument("--quick", action="store_true",
                     help="time the step only: no variants, end-to-end or CPU baseline")
     args = ap.parse_args(argv)
@@ -646,6 +853,8 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif (world > 1 and not args.replicas) or args.zero1:
+        line = run_zero1(args, world, rank, local)
     else:
         line = run_ours(args, world, rank, local)
     if line is not None:

@@ -129,6 +129,82 @@ int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip,
                  void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The norm in two halves, for ZeRO-1 — [LLMC] §4: under ZeRO-1 each rank
+ * takes the sum of squares of its own gradient shard only (after the
+ * reduce-scatter of §3.2), and the per-rank sums are combined across ranks
+ * before the clip scale is taken; [CMU13] §5.2: ZeRO-1 computes what data
+ * parallelism computes.
+ *
+ * mp_grad_sumsq: sumsq of grads[0, n) exactly as mp_grad_norm computes it
+ * (the same kernels, the same bits), written to *d_sumsq; no norm or scale.
+ *   grads, n, workspace, workspace_bytes, stream   as mp_grad_norm.
+ *   d_sumsq   double[1], device, written.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_WORKSPACE,
+ *         MP_ERR_CUDA.
+ *
+ * mp_clip_scale_from_sumsq: combines `count` sums of squares (one per rank,
+ * gathered by the caller's collective into d_sumsq[0..count) in rank order):
+ *   S     = d_sumsq[0] + d_sumsq[1] + ... + d_sumsq[count-1]
+ *           (fp64, left to right: every rank that passes the same values gets
+ *           the same bits, whatever its own rank)
+ *   norm  = (float) sqrt(S);   scale = as mp_grad_norm (NaN if norm is not
+ *           finite, else min(1, clip / norm))
+ * With count == 1 and mp_grad_sumsq's output this is mp_grad_norm's result.
+ *   d_sumsq   double[count], device, read only.
+ *   count     1 .. 2^20.
+ *   clip      finite and > 0.
+ *   d_norm, d_scale   float[1], device, written.
+ *   d_total   double[1], device, written (S); may be NULL.
+ * One single-thread kernel; nothing is allocated.
+ * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_grad_sumsq(const uint16_t* grads, uint64_t n, void* workspace, size_t workspace_bytes,
+                  double* d_sumsq, void* stream);
+
+int mp_clip_scale_from_sumsq(const double* d_sumsq, int32_t count, float clip,
+                             float* d_norm, float* d_scale, double* d_total, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Learning-rate schedules — [LLMC] §4 names four (cosine, linear, constant,
+ * WSD) and prints no formula. The learning rate of the 1-based step t (the t
+ * mp_adamw_step takes), computed on the host in double and rounded to float
+ * once:
+ *   t <= warmup:  lr_max * t / warmup                      (linear warm-up)
+ *   afterwards, p = min(1, (t - warmup) / (total - warmup)):
+ *     MP_LR_CONSTANT  lr_max
+ *     MP_LR_COSINE    lr_min + (lr_max - lr_min) * (1 + cos(pi * p)) / 2
+ *     MP_LR_LINEAR    lr_max - (lr_max - lr_min) * p
+ *     MP_LR_WSD       lr_max while p <= 1 - decay_frac (warm-up, stable),
+ *                     then lr_max - (lr_max - lr_min) * (p - (1 - decay_frac))
+ *                     / decay_frac: linear to lr_min over the last fraction
+ * Steps past `total` keep the last value. Host only; no CUDA call.
+ *   s    host struct: kind, warmup >= 0, total > warmup (not used by
+ *        MP_LR_CONSTANT), finite lr_max and lr_min, decay_frac in (0, 1]
+ *        (MP_LR_WSD only), reserved fields 0.
+ *   t    >= 1.
+ *   lr   host float[1], written.
+ * Errors: MP_ERR_NULL, MP_ERR_RANGE (invalid schedule or t < 1).
+ * ------------------------------------------------------------------------- */
+typedef enum mp_lr_kind {
+    MP_LR_CONSTANT = 0,
+    MP_LR_COSINE = 1,
+    MP_LR_LINEAR = 2,
+    MP_LR_WSD = 3
+} mp_lr_kind_t;
+
+typedef struct mp_lr_schedule {
+    int32_t kind;      /* mp_lr_kind_t */
+    int32_t reserved;  /* must be 0 */
+    int64_t warmup;    /* warm-up steps */
+    int64_t total;     /* steps of the run */
+    float lr_max, lr_min;
+    float decay_frac;  /* MP_LR_WSD: fraction of the post-warm-up steps that decays */
+    float reserved2;   /* must be 0 (not checked) */
+} mp_lr_schedule_t;
+
+int mp_lr_at(const mp_lr_schedule_t* s, int64_t t, float* lr);
+
+/* ---------------------------------------------------------------------------
  * AdamW step with stochastic-rounding write-back — [LLMC] §2.2 (update),
  * §2.3 (rounding), §4 (t = step + 1); [CMU13] §1.7 (bias correction,
  * decoupled decay).
@@ -452,7 +528,11 @@ int mp_optimizer_step_graph(uint16_t* params, uint16_t* grads, const uint16_t* h
  *
  * The first call on a device looks up the scratch array's device address
  * (with that device current) and caches it; make that first call before any
- * stream capture. The scratch is shared by all calls on a device and keeps
+ * stream capture. The cached address belongs to the device's primary
+ * context: it assumes that context for the life of the process (no
+ * cudaDeviceReset, no other driver context made current on that device).
+ * Devices with an ordinal of 64 or more are looked up on every call. The
+ * scratch is shared by all calls on a device and keeps
  * the last call's contents (each call overwrites every slot it reads, so
  * nothing needs clearing): calls that overlap on the GPU — on two streams,
  * or from two threads without ordering — race on it and must be serialised

@@ -56,6 +56,13 @@ class MpLaunch(ctypes.Structure):
                 ("first_decay", ctypes.c_uint32)]
 
 
+class MpLrSchedule(ctypes.Structure):
+    """mp_lr_schedule_t: a learning-rate schedule (mp_lr_at)."""
+    _fields_ = [("kind", ctypes.c_int32), ("reserved", ctypes.c_int32), ("warmup", ctypes.c_int64),
+                ("total", ctypes.c_int64), ("lr_max", ctypes.c_float), ("lr_min", ctypes.c_float),
+                ("decay_frac", ctypes.c_float), ("reserved2", ctypes.c_float)]
+
+
 class MpStepState(ctypes.Structure):
     """mp_step_state_t: the device step counter of replayable steps (32 B)."""
     _fields_ = [("t", ctypes.c_int32), ("seed_base", ctypes.c_uint32), ("lr", ctypes.c_float),
@@ -80,6 +87,12 @@ def _load():
     L.mp_grad_norm_workspace_bytes.argtypes = [u64]
     L.mp_grad_norm.restype = ctypes.c_int
     L.mp_grad_norm.argtypes = [vp, u64, f32, vp, ctypes.c_size_t, vp, vp, vp, vp]
+    L.mp_grad_sumsq.restype = ctypes.c_int
+    L.mp_grad_sumsq.argtypes = [vp, u64, vp, ctypes.c_size_t, vp, vp]
+    L.mp_clip_scale_from_sumsq.restype = ctypes.c_int
+    L.mp_clip_scale_from_sumsq.argtypes = [vp, i32, f32, vp, vp, vp, vp]
+    L.mp_lr_at.restype = ctypes.c_int
+    L.mp_lr_at.argtypes = [ctypes.POINTER(MpLrSchedule), ctypes.c_int64, ctypes.POINTER(ctypes.c_float)]
     L.mp_adamw_step.restype = ctypes.c_int
     L.mp_adamw_step.argtypes = [vp, vp, vp, vp, vp, u64, u64, ctypes.POINTER(MpTensor), i32,
                                 f32, f32, f32, f32, f32, vp, i32, u32, vp, vp]
@@ -208,6 +221,55 @@ def mp_grad_norm(grads: torch.Tensor, clip: float, workspace: torch.Tensor, d_no
         _ptr(d_norm, (torch.float32,), "d_norm", 1), _ptr(d_scale, (torch.float32,), "d_scale", 1),
         _ptr(d_sumsq, (torch.float64,), "d_sumsq", 1), _stream(stream))
     _check(st, "mp_grad_norm")
+
+
+def mp_grad_sumsq(grads: torch.Tensor, workspace: torch.Tensor, d_sumsq: torch.Tensor, n: Optional[int] = None,
+                  stream=None) -> None:
+    """Enqueue the sum of squares of grads (mp_grad_norm's, bit for bit)
+    into the device double d_sumsq: one rank's share of a ZeRO-1 norm."""
+    n = grads.numel() if n is None else n
+    st = _lib.mp_grad_sumsq(
+        _ptr(grads, _BF16_LIKE, "grads", n), n,
+        _ptr(workspace, (torch.uint8, torch.float64, torch.int64), "workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(d_sumsq, (torch.float64,), "d_sumsq", 1),
+        _stream(stream))
+    _check(st, "mp_grad_sumsq")
+
+
+def mp_clip_scale_from_sumsq(d_sumsq: torch.Tensor, clip: float, d_norm: torch.Tensor, d_scale: torch.Tensor,
+                             d_total: Optional[torch.Tensor] = None, count: Optional[int] = None,
+                             stream=None) -> None:
+    """Enqueue the norm and clip scale from `count` per-rank sums of squares
+    (device float64, rank order), added left to right in fp64."""
+    count = d_sumsq.numel() if count is None else count
+    st = _lib.mp_clip_scale_from_sumsq(
+        _ptr(d_sumsq, (torch.float64,), "d_sumsq", count), count, clip,
+        _ptr(d_norm, (torch.float32,), "d_norm", 1), _ptr(d_scale, (torch.float32,), "d_scale", 1),
+        _ptr(d_total, (torch.float64,), "d_total", 1), _stream(stream))
+    _check(st, "mp_clip_scale_from_sumsq")
+
+
+LR_KINDS = {"constant": 0, "cosine": 1, "linear": 2, "wsd": 3}
+
+
+class LRSchedule:
+    """A learning-rate schedule of the library (mp_lr_at): linear warm-up,
+    then constant, cosine, linear or WSD (warm-up, stable, decay)."""
+
+    def __init__(self, kind: str, *, lr_max: float, lr_min: float = 0.0, warmup: int = 0, total: int = 0,
+                 decay_frac: float = 0.0):
+        if kind not in LR_KINDS:
+            raise ValueError(f"kind: one of {sorted(LR_KINDS)}")
+        self.kind = kind
+        self._s = MpLrSchedule(LR_KINDS[kind], 0, int(warmup), int(total), float(lr_max), float(lr_min),
+                               float(decay_frac), 0.0)
+        self.lr(max(1, int(warmup) + 1))  # validates the schedule
+
+    def lr(self, t: int) -> float:
+        """Learning rate of the 1-based step t."""
+        out = ctypes.c_float()
+        _check(_lib.mp_lr_at(ctypes.byref(self._s), int(t), ctypes.byref(out)), "mp_lr_at")
+        return out.value
 
 
 def mp_grad_norm_noalloc(grads: torch.Tensor, clip: float, d_norm: torch.Tensor, d_scale: torch.Tensor,
@@ -425,8 +487,9 @@ class Optimizer:
 
     def __init__(self, table_entries: Sequence[Tuple[int, int, int]], *, lr: float, beta1: float,
                  beta2: float, eps: float, weight_decay: float, clip: float, device=None,
-                 outlier_z: Optional[float] = None):
+                 outlier_z: Optional[float] = None, schedule: Optional[LRSchedule] = None):
         self.table = TensorTable(table_entries)
+        self.schedule = schedule
         self.n = self.table.total
         self.hyper = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay)
         self.clip = clip
@@ -443,7 +506,10 @@ class Optimizer:
 
     def step(self, params, grads, master, m, v, t: int, seed: int, host_grads=None, host_norm=None, stream=None):
         """One native call (mp_optimizer_step). With host_grads (pinned CPU
-        bf16), `grads` is the device buffer that receives them."""
+        bf16), `grads` is the device buffer that receives them. With a
+        schedule, step t uses the schedule's learning rate for t."""
+        if self.schedule is not None:
+            self.hyper_struct.lr = self.schedule.lr(t)
         mp_optimizer_step(params, grads, master, m, v, self.table, self.hyper_struct, t=t, seed=seed,
                           workspace=self.workspace, d_norm=self.d_norm, d_scale=self.d_scale,
                           d_status=self.d_status,
@@ -519,5 +585,6 @@ __all__ = [
     "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
     "mp_stochastic_round", "mp_stochastic_round_fp16", "mp_accumulate_sr", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
-    "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH",
+    "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH", "mp_grad_sumsq", "mp_clip_scale_from_sumsq",
+    "LRSchedule", "MpLrSchedule", "LR_KINDS",
 ]

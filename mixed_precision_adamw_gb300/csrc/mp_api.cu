@@ -33,6 +33,10 @@ bool beta_ok(float beta) { return beta >= 0.0f && beta < 1.0f; }
 
 constexpr int64_t kMaxBiasLen = int64_t{1} << 26;
 
+constexpr int32_t kMaxSumsqParts = 1 << 20;  // per-rank sums one scale call adds
+
+constexpr double kPi = 3.141592653589793;  // the double nearest pi
+
 }  // namespace
 
 namespace mpk {
@@ -103,6 +107,72 @@ int mp_grad_norm(const uint16_t* grads, uint64_t n, float clip, void* workspace,
   e = mpk::launch_norm(grads, n, vec, static_cast<double*>(workspace), nb, clip, d_norm, d_scale, d_sumsq,
                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_grad_sumsq(const uint16_t* grads, uint64_t n, void* workspace, size_t workspace_bytes, double* d_sumsq,
+                  void* stream) {
+  if ((n != 0 && grads == nullptr) || d_sumsq == nullptr) return MP_ERR_NULL;
+  if (workspace == nullptr) return MP_ERR_WORKSPACE;
+  if (!aligned(grads, 2) || !aligned(workspace, 8) || !aligned(d_sumsq, 8)) return MP_ERR_ALIGN;
+  if (n > kMaxN) return MP_ERR_RANGE;
+  mpk::DeviceInfo dev;
+  cudaError_t e = mpk::device_info(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const bool vec = aligned(grads, 16);
+  const int nb = mpk::norm_blocks(n, vec, dev);
+  if (workspace_bytes < sizeof(double) * static_cast<size_t>(nb)) return MP_ERR_WORKSPACE;
+  e = mpk::launch_norm(grads, n, vec, static_cast<double*>(workspace), nb, 1.0f, nullptr, nullptr, d_sumsq,
+                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_clip_scale_from_sumsq(const double* d_sumsq, int32_t count, float clip, float* d_norm, float* d_scale,
+                             double* d_total, void* stream) {
+  if (d_sumsq == nullptr || d_norm == nullptr || d_scale == nullptr) return MP_ERR_NULL;
+  if (!aligned(d_sumsq, 8) || !aligned(d_norm, 4) || !aligned(d_scale, 4) || !aligned(d_total, 8))
+    return MP_ERR_ALIGN;
+  if (count < 1 || count > kMaxSumsqParts || !(clip > 0.0f) || !std::isfinite(clip)) return MP_ERR_RANGE;
+  const cudaError_t e = mpk::launch_scale_from_sumsq(d_sumsq, count, clip, d_norm, d_scale, d_total,
+                                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MP_OK;
+}
+
+int mp_lr_at(const mp_lr_schedule_t* s, int64_t t, float* lr) {
+  if (s == nullptr || lr == nullptr) return MP_ERR_NULL;
+  const bool decays = s->kind != MP_LR_CONSTANT;
+  if (s->kind < MP_LR_CONSTANT || s->kind > MP_LR_WSD || s->reserved != 0 || s->warmup < 0 || t < 1 ||
+      (decays && s->total <= s->warmup) || !std::isfinite(s->lr_max) || !std::isfinite(s->lr_min) ||
+      (s->kind == MP_LR_WSD && !(s->decay_frac > 0.0f && s->decay_frac <= 1.0f)))
+    return MP_ERR_RANGE;
+  const double peak = s->lr_max, floor_lr = s->lr_min;
+  if (t <= s->warmup) {  // linear warm-up, reaching the peak at t = warmup
+    *lr = static_cast<float>(peak * static_cast<double>(t) / static_cast<double>(s->warmup));
+    return MP_OK;
+  }
+  if (!decays) {
+    *lr = s->lr_max;
+    return MP_OK;
+  }
+  const double span = static_cast<double>(s->total - s->warmup);
+  const double p = std::fmin(1.0, static_cast<double>(t - s->warmup) / span);  // progress after warm-up
+  double out = peak;
+  switch (s->kind) {
+    case MP_LR_COSINE:
+      out = floor_lr + (peak - floor_lr) * (1.0 + std::cos(kPi * p)) / 2.0;
+      break;
+    case MP_LR_LINEAR:
+      out = peak - (peak - floor_lr) * p;
+      break;
+    default: {  // MP_LR_WSD: stable, then linear over the last fraction
+      const double f = s->decay_frac, start = 1.0 - f;
+      out = p <= start ? peak : peak - (peak - floor_lr) * (p - start) / f;
+      break;
+    }
+  }
+  *lr = static_cast<float>(out);
   return MP_OK;
 }
 

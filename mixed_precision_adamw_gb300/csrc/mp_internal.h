@@ -93,10 +93,16 @@ int norm_blocks(uint64_t n, bool vec, const DeviceInfo& dev);
 // copy_out != nullptr: grads may be page-locked host memory (device-visible
 // address); the kernel also writes every gradient to copy_out (device).
 // clock != nullptr: the finalize kernel also advances the device step counter.
+// d_norm == nullptr (then d_scale and clock are unused): only d_sumsq is written.
 cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* partials,
                         int nblocks, float clip, float* d_norm, float* d_scale,
                         double* d_sumsq, cudaStream_t stream, uint16_t* copy_out = nullptr,
                         const StepClock* clock = nullptr);
+
+// ZeRO-1 norm: norm and scale from `count` per-rank sums of squares, added
+// in index order in fp64 (one thread).
+cudaError_t launch_scale_from_sumsq(const double* parts, int count, float clip, float* d_norm, float* d_scale,
+                                    double* d_total, cudaStream_t stream);
 
 // One-launch step for small parameter sets (mp_small.cu): a cluster of
 // kSmallClusterCtas CTAs runs the norm, the optional outlier check and the

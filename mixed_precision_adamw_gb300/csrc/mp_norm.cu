@@ -16,6 +16,7 @@
 // The grid and the element mapping depend only on n, the SM count and whether
 // the gradients are 16-B aligned (8-element vectors) or not (single
 // elements): results are bit-identical across runs.
+#include <atomic>
 #include <cmath>
 
 #include "mp_adamw.h"
@@ -46,15 +47,34 @@ norm_finalize_kernel(const double* __restrict__ partials, int nb, float clip,
   pdl_enter();
   const double S = norm_total([partials](int i) { return partials[i]; }, nb, sh);
   if (threadIdx.x == 0) {
+    if (d_norm != nullptr) {  // null: the sum of squares alone (mp_grad_sumsq)
+      float norm, scale;
+      norm_and_scale(S, clip, norm, scale);
+      if (clock.state != nullptr && !advance_clock(clock)) {
+        scale = __int_as_float(0x7FC00000);
+        if (clock.d_status != nullptr) atomicCAS(clock.d_status, 0, MP_ERR_RANGE);
+      }
+      *d_norm = norm;
+      *d_scale = scale;
+    }
+    if (d_sumsq != nullptr) *d_sumsq = S;
+  }
+}
+
+// The norm and clip scale from `count` sums of squares (one per ZeRO-1
+// rank), added in index order in fp64 by one thread.
+__global__ void __launch_bounds__(32)
+scale_from_sumsq_kernel(const double* __restrict__ parts, int count, float clip, float* d_norm, float* d_scale,
+                        double* d_total) {
+  pdl_enter();
+  if (threadIdx.x == 0) {
+    double S = 0.0;
+    for (int r = 0; r < count; ++r) S = __dadd_rn(S, parts[r]);
     float norm, scale;
     norm_and_scale(S, clip, norm, scale);
-    if (clock.state != nullptr && !advance_clock(clock)) {
-      scale = __int_as_float(0x7FC00000);
-      if (clock.d_status != nullptr) atomicCAS(clock.d_status, 0, MP_ERR_RANGE);
-    }
     *d_norm = norm;
     *d_scale = scale;
-    if (d_sumsq != nullptr) *d_sumsq = S;
+    if (d_total != nullptr) *d_total = S;
   }
 }
 
@@ -83,6 +103,11 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
                     clip, d_norm, d_scale, d_sumsq, c);
 }
 
+cudaError_t launch_scale_from_sumsq(const double* parts, int count, float clip, float* d_norm, float* d_scale,
+                                    double* d_total, cudaStream_t stream) {
+  return launch_pdl(scale_from_sumsq_kernel, 1u, 32u, stream, parts, count, clip, d_norm, d_scale, d_total);
+}
+
 }  // namespace mpk
 
 // ---------------------------------------------------------------------------
@@ -101,16 +126,20 @@ static __device__ __align__(256) double g_norm_scratch[kNoAllocMaxPartials];
 // Device address of g_norm_scratch, looked up once per device (with that
 // device current) on the first call made on it. In host code the array's name
 // is only a host-side stand-in, never a device address, so it is not passed
-// to a kernel directly.
-void* g_scratch_addr[64];
+// to a kernel directly. The cache is keyed by device ordinal and assumes that
+// device's primary context for the life of the process (no cudaDeviceReset).
+// Ordinals past the cache are looked up on every call.
+constexpr int kAddrCache = 64;
+std::atomic<void*> g_scratch_addr[kAddrCache];
 
 cudaError_t scratch_address(int device, double** out) {
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[device];
+  const bool cached = device >= 0 && device < kAddrCache;
+  void* p = cached ? g_scratch_addr[device].load(std::memory_order_relaxed) : nullptr;
   if (p == nullptr) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_norm_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[device] = p;  // racing first calls store the same address
+    // racing first calls on one device store the same address
+    if (cached) g_scratch_addr[device].store(p, std::memory_order_relaxed);
   }
   *out = static_cast<double*>(p);
   return cudaSuccess;

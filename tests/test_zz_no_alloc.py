@@ -3,15 +3,18 @@ device memory (a framework that owns all of it and hands over only tensors,
 or a loop that cannot take cudaMalloc's device-wide synchronisation).
 
 It must give what mp_grad_norm gives on the same inputs, call after call,
-although its partial sums live in a scratch array shared by every call. This
-file is collected last, so a run that stops at its first failure has already
-run every other test; it also passes on its own in a fresh process.
+although its partial sums live in a scratch array shared by every call, and
+its sum of squares must meet the norm's bar against the oracle's fp64 sum.
+This file is collected last, so a run that stops at its first failure has
+already run every other test; it also passes on its own in a fresh process.
 """
 import ctypes
 
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -40,11 +43,15 @@ def _with_workspace(mp, g):
     return out
 
 
+def _fresh_outputs():
+    return (torch.full((1,), -1.0, dtype=torch.float32, device="cuda"),
+            torch.full((1,), -1.0, dtype=torch.float32, device="cuda"),
+            torch.full((1,), -1.0, dtype=torch.float64, device="cuda"))
+
+
 def _without_workspace(mp, g):
     """Straight through the C ABI with raw device pointers."""
-    out = (torch.full((1,), -1.0, dtype=torch.float32, device="cuda"),
-           torch.full((1,), -1.0, dtype=torch.float32, device="cuda"),
-           torch.full((1,), -1.0, dtype=torch.float64, device="cuda"))
+    out = _fresh_outputs()
     st = mp.lib().mp_grad_norm_noalloc(
         ctypes.c_void_p(g.data_ptr()), g.numel(), ctypes.c_float(1.0), ctypes.c_void_p(out[0].data_ptr()),
         ctypes.c_void_p(out[1].data_ptr()), ctypes.c_void_p(out[2].data_ptr()),
@@ -53,19 +60,36 @@ def _without_workspace(mp, g):
     return out
 
 
-def test_noalloc_norm_matches_workspace_norm_on_two_calls_in_a_row(mp):
-    # two different inputs back to back: a large one (many blocks, every
-    # scratch slot in use) then a smaller one that reuses fewer slots
-    for n, seed, scale in ((50_000_003, 1, 1e-3), (3 * 2048 + 5, 2, 7.0)):
-        g = _grads(n, seed, scale)
+def _through_binding(mp, g):
+    """The Python wrapper of the same entry point."""
+    out = _fresh_outputs()
+    mp.mp_grad_norm_noalloc(g, 1.0, out[0], out[1], out[2])
+    return out
+
+
+def _host_bits(g):
+    return g.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("call", [_without_workspace, _through_binding])
+def test_noalloc_norm_matches_workspace_norm_on_two_calls_in_a_row(mp, call):
+    # Back to back: a large input (every scratch slot this device's grid
+    # uses), a small one that reuses fewer slots, and a 2-byte-aligned view
+    # (the element-by-element path, whose grid and mapping differ).
+    big = _grads(50_000_003, 1, 1e-3)
+    cases = [big, _grads(3 * 2048 + 5, 2, 7.0), big[1:1_000_001]]
+    for g in cases:
         ref = _with_workspace(mp, g)
-        got = _without_workspace(mp, g)
+        got = call(mp, g)
         torch.cuda.synchronize()
         norm_r, scale_r, sumsq_r = (x.item() for x in ref)
         norm_g, scale_g, sumsq_g = (x.item() for x in got)
-        # the bar the norm tests use: relative error <= 1e-6 (here the same
-        # kernels run, so the results are expected to be identical)
+        # the bar the norm tests use: relative error <= 1e-6 against the
+        # oracle's fp64 sum of squares in index order
+        sumsq_o = oracle.sumsq(_host_bits(g))
+        assert abs(sumsq_g - sumsq_o) <= 1e-6 * abs(sumsq_o)
+        assert abs(norm_g - np.sqrt(sumsq_o)) <= 1e-6 * np.sqrt(sumsq_o)
+        # the same kernels as mp_grad_norm: identical results expected
         assert abs(sumsq_g - sumsq_r) <= 1e-6 * abs(sumsq_r)
-        assert abs(norm_g - norm_r) <= 1e-6 * abs(norm_r)
         assert np.float32(scale_g) == np.float32(scale_r)
         assert (norm_g, scale_g, sumsq_g) == (norm_r, scale_r, sumsq_r)
