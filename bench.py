@@ -301,6 +301,11 @@ def run_ours(args, world, rank, local):
         roofline["copy_ceiling"] = ceiling
         variants = measure_variants(mp, st, grads[0], opt, N, entries, tab, stream, device, peak)
         e2e = measure_e2e(mp, st, grads[0], opt, N, stream, device, kw, min(args.steps, 200), step_no)
+        # last: the probes overwrite the bf16 weights
+        probes = measure_stream_probes(st, grads[0], N, stream, peak)
+        best = max(v["gbs"] for k, v in probes.items() if k.startswith("step_streams"))
+        probes["step_kernel_frac_of_best_step_streams"] = round(achieved / best, 4)
+        roofline["sm_stream_probes"] = probes
 
     if rank != 0:
         return None
@@ -549,6 +554,47 @@ def measure_variants(mp, st, g, opt, N, entries, tab, stream, device, peak):
     ms = time_events(shards, iters // 2, stream)
     out["step_8_shards"] = {**LAST_TIMING, "ms": round(ms, 5), "gparams_s": round(N / ms / 1e6, 2),
                             "gbs": round(STEP_BYTES_MASTER * N / ms / 1e6, 1), "launches": 8}
+    return out
+
+
+def measure_stream_probes(st, g, N, stream, peak):
+    """Compute-free probes (libmpprobe.so, measurement only): the step's five
+    streams with its tiling, vector widths, cache hints and occupancy, values
+    written back unchanged; and a plain 16-B vector copy of 4 GiB. They give
+    the practical ceiling of kernels on the SMs for this read/write mix,
+    beside the copy engines' figure (copy_ceiling)."""
+    import ctypes
+    lib = ctypes.CDLL(os.path.join(ROOT, "mixed_precision_adamw_gb300", "libmpprobe.so"))
+    vp, u64, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int
+    lib.mp_probe_step_streams.argtypes = [vp, vp, vp, vp, vp, u64, i32, vp]
+    lib.mp_probe_copy.argtypes = [vp, vp, u64, i32, vp]
+    chunk = 201_326_592  # the step's launch size on the large sets (whole 2048-element tiles)
+    n = N // 2048 * 2048
+    out = {}
+    for bps in (3, 4, 8):
+        def run():
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                rc = lib.mp_probe_step_streams(st["params"][a:].data_ptr(), g[a:].data_ptr(),
+                                               st["master"][a:].data_ptr(), st["m"][a:].data_ptr(),
+                                               st["v"][a:].data_ptr(), b - a, bps, stream.cuda_stream)
+                assert rc == 0, rc
+        ms = time_events(run, 5, stream)
+        out[f"step_streams_{bps}_blocks_per_sm"] = {"gbs": round(STEP_BYTES_MASTER * n / ms / 1e6, 1),
+                                                    "frac": round(STEP_BYTES_MASTER * n / ms / 1e6 / peak, 4),
+                                                    "ms": round(ms, 5)}
+    nbytes = min(STEP_BYTES_MASTER // 2 * N, 1 << 32) // 16 * 16
+    src = torch.empty(nbytes, dtype=torch.uint8, device=g.device)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    for bps in (4, 8):
+        ms = time_events(lambda: lib.mp_probe_copy(dst.data_ptr(), src.data_ptr(), nbytes // 16, bps,
+                                                   stream.cuda_stream), 10, stream)
+        out[f"copy_16B_{bps}_blocks_per_sm"] = {"gbs": round(2 * nbytes / ms / 1e6, 1),
+                                                "frac": round(2 * nbytes / ms / 1e6 / peak, 4), "ms": round(ms, 5)}
+    del src, dst
+    out["what"] = ("compute-free SM kernels: the step's streams (28 B/param, written back unchanged) in "
+                   f"launches of {chunk} params, and a 16-B copy of {nbytes} bytes")
     return out
 
 

@@ -18,8 +18,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmpadamw.so")
+# compute-free stream probes, a separate library that only the benchmark loads
+PROBE_LIB = os.path.join(PKG, "libmpprobe.so")
 
 SOURCES = ["mp_api.cu", "mp_step.cu", "mp_norm.cu", "mp_sr.cu", "mp_outlier.cu", "mp_small.cu"]
+PROBE_SOURCES = ["mp_probe.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
     "-O3", "-std=c++17", "-lineinfo", *GENCODE,
@@ -45,9 +48,9 @@ def _inputs():
 
 
 def is_stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PROBE_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
@@ -68,15 +71,20 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES) + len(PROBE_SOURCES)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES + PROBE_SOURCES))
+    _link(objs[:len(SOURCES)], LIB)
+    _link(objs[len(SOURCES):], PROBE_LIB)
+    return LIB
+
+
+def _link(objs, out):
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), "-shared", *GENCODE, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
 
 
 if __name__ == "__main__":

@@ -42,9 +42,13 @@ __device__ __forceinline__ uint32_t noise_pos(uint64_t k) {
   return static_cast<uint32_t>(k) + kNoisePrime * static_cast<uint32_t>(k >> 32);
 }
 
-// Every SquirrelNoise5 round except the final xor-shift by 17.
-__device__ __forceinline__ uint32_t noise_rounds(uint32_t pos, uint32_t seed) {
-  uint32_t h = pos * 0xD2A80A3Fu + seed;
+constexpr uint32_t kNoiseMul1 = 0xD2A80A3Fu;   // the first round's multiplier
+
+// The first SquirrelNoise5 round: pos * C1 + seed.
+__device__ __forceinline__ uint32_t noise_first(uint32_t pos, uint32_t seed) { return pos * kNoiseMul1 + seed; }
+
+// Every round after the first, except the final xor-shift by 17.
+__device__ __forceinline__ uint32_t noise_rest(uint32_t h) {
   h ^= h >> 9;
   h += 0xA884F197u;
   h ^= h >> 11;
@@ -56,15 +60,25 @@ __device__ __forceinline__ uint32_t noise_rounds(uint32_t pos, uint32_t seed) {
   return h;
 }
 
+// Every SquirrelNoise5 round except the final xor-shift by 17.
+__device__ __forceinline__ uint32_t noise_rounds(uint32_t pos, uint32_t seed) {
+  return noise_rest(noise_first(pos, seed));
+}
+
 __device__ __forceinline__ uint32_t noise_u32(uint64_t k, uint32_t seed) {
   const uint32_t h = noise_rounds(noise_pos(k), seed);
   return h ^ (h >> 17);
 }
 
-// 0xFFFF minus the 16-bit draw (the low half of the noise), i.e. ~draw & 0xFFFF.
-__device__ __forceinline__ uint32_t draw16_complement(uint32_t pos, uint32_t seed) {
-  const uint32_t h = noise_rounds(pos, seed);
+// 0xFFFF minus the 16-bit draw (the low half of the noise), i.e. ~draw & 0xFFFF,
+// from the first round's value h1 = noise_first(pos, seed).
+__device__ __forceinline__ uint32_t draw16_complement_h1(uint32_t h1) {
+  const uint32_t h = noise_rest(h1);
   return ~(h ^ (h >> 17)) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint32_t draw16_complement(uint32_t pos, uint32_t seed) {
+  return draw16_complement_h1(noise_first(pos, seed));
 }
 
 // Noise positions of the 4 consecutive indices k0 .. k0+3 from one fold:
@@ -76,6 +90,36 @@ __device__ __forceinline__ void noise_pos4(uint64_t k0, uint32_t (&pos)[4]) {
   const uint32_t p0 = noise_pos(k0);
 #pragma unroll
   for (int j = 0; j < 4; ++j) pos[j] = p0 + j + (lo > 0xFFFFFFFFu - j ? kNoisePrime : 0u);
+}
+
+// First-round values h1[j] = noise_first(noise_pos(k0 + j), seed) of the 4
+// consecutive indices k0 .. k0+3. When their low words do not wrap past 2^32
+// (all but one group in 2^30), noise_pos(k0 + j) = noise_pos(k0) + j, so
+// h1[j] = h1[0] + j * C1 (mod 2^32): one multiply-add for the group and one
+// constant addition per further element, instead of a position, a wrap test
+// and a multiply-add per element. The rare wrapping group takes noise_pos4.
+__device__ __forceinline__ void noise_first4(uint64_t k0, uint32_t seed, uint32_t (&h1)[4]) {
+  if (static_cast<uint32_t>(k0) <= 0xFFFFFFFCu) {
+    const uint32_t b = noise_first(noise_pos(k0), seed);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h1[j] = b + static_cast<uint32_t>(j) * kNoiseMul1;
+  } else {
+    uint32_t pos[4];
+    noise_pos4(k0, pos);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h1[j] = noise_first(pos[j], seed);
+  }
+}
+
+// True when none of the 8 values is NaN: their sum is then not NaN unless
+// infinities of both signs meet, which only sends such a group to the path
+// that checks every element. The additions run on the FMA pipe, which the
+// rounding kernels leave mostly idle, instead of a compare and a select per
+// element on the integer pipe.
+__device__ __forceinline__ bool none_nan8(const float4& a, const float4& b) {
+  const float s = __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w)),
+                            __fadd_rn(__fadd_rn(b.x, b.y), __fadd_rn(b.z, b.w)));
+  return s == s;
 }
 
 // ---- stochastic rounding fp32 -> bf16 -------------------------------------
@@ -105,6 +149,32 @@ __device__ __forceinline__ uint32_t sr_bf16_hi(float x, uint32_t draw_complement
 // 2, 3 of hi_word.
 __device__ __forceinline__ uint32_t pack_hi16(uint32_t lo_word, uint32_t hi_word) {
   return __byte_perm(lo_word, hi_word, 0x7632);
+}
+
+// Stochastic rounding of a thread's two 4-element groups a (global indices
+// k0 .. k0+3) and b (k1 .. k1+3), packed as bf16 pairs. Without NaN among
+// the 8 values (none_nan8) each result is the high half of b + c, with no
+// per-element NaN select; otherwise sr_bf16_hi per element.
+__device__ __forceinline__ void sr_pack8(const float4& a, const float4& b, uint64_t k0, uint64_t k1, uint32_t seed,
+                                         uint2& qa, uint2& qb) {
+  uint32_t ha[4], hb[4];
+  noise_first4(k0, seed, ha);
+  noise_first4(k1, seed, hb);
+  if (none_nan8(a, b)) {
+    qa.x = pack_hi16(__float_as_uint(a.x) + draw16_complement_h1(ha[0]),
+                     __float_as_uint(a.y) + draw16_complement_h1(ha[1]));
+    qa.y = pack_hi16(__float_as_uint(a.z) + draw16_complement_h1(ha[2]),
+                     __float_as_uint(a.w) + draw16_complement_h1(ha[3]));
+    qb.x = pack_hi16(__float_as_uint(b.x) + draw16_complement_h1(hb[0]),
+                     __float_as_uint(b.y) + draw16_complement_h1(hb[1]));
+    qb.y = pack_hi16(__float_as_uint(b.z) + draw16_complement_h1(hb[2]),
+                     __float_as_uint(b.w) + draw16_complement_h1(hb[3]));
+  } else {
+    qa.x = pack_hi16(sr_bf16_hi(a.x, draw16_complement_h1(ha[0])), sr_bf16_hi(a.y, draw16_complement_h1(ha[1])));
+    qa.y = pack_hi16(sr_bf16_hi(a.z, draw16_complement_h1(ha[2])), sr_bf16_hi(a.w, draw16_complement_h1(ha[3])));
+    qb.x = pack_hi16(sr_bf16_hi(b.x, draw16_complement_h1(hb[0])), sr_bf16_hi(b.y, draw16_complement_h1(hb[1])));
+    qb.y = pack_hi16(sr_bf16_hi(b.z, draw16_complement_h1(hb[2])), sr_bf16_hi(b.w, draw16_complement_h1(hb[3])));
+  }
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -66,21 +66,22 @@ __device__ __forceinline__ uint32_t sr_fp16_hi_normal(float x, uint32_t draw_com
   return ((b << 3) + 0x40000000u + draw_complement) | (b & 0x80000000u);
 }
 
-// Four consecutive elements at noise positions pos[0..3], packed as fp16.
+// Four consecutive elements with first-round noise values h1[0..3], packed
+// as fp16.
 template <bool kNormalOnly>
-__device__ __forceinline__ uint2 sr_fp16_pack4(const float4& x, const uint32_t (&pos)[kGroup], uint32_t seed) {
-  auto r = [&](float v, uint32_t p) {
-    return kNormalOnly ? sr_fp16_hi_normal(v, draw16_complement(p, seed)) : sr_fp16_hi(v, draw16_complement(p, seed));
+__device__ __forceinline__ uint2 sr_fp16_pack4(const float4& x, const uint32_t (&h1)[kGroup]) {
+  auto r = [&](float v, uint32_t h) {
+    return kNormalOnly ? sr_fp16_hi_normal(v, draw16_complement_h1(h)) : sr_fp16_hi(v, draw16_complement_h1(h));
   };
   uint2 q;
-  q.x = pack_hi16(r(x.x, pos[0]), r(x.y, pos[1]));
-  q.y = pack_hi16(r(x.z, pos[2]), r(x.w, pos[3]));
+  q.x = pack_hi16(r(x.x, h1[0]), r(x.y, h1[1]));
+  q.y = pack_hi16(r(x.z, h1[2]), r(x.w, h1[3]));
   return q;
 }
 
 // Vector path: in 16-B aligned, out 8-B aligned. Same tiling as the step:
 // thread t converts the 4-element groups at tile offsets 4t and 4t + 1024.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kSrBlocksPerSm)
 sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n, uint32_t seed) {
   pdl_enter();
   const uint64_t ntiles = n / kTile;
@@ -89,14 +90,8 @@ sr_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t
     const uint64_t e1 = e0 + kThreads * kGroup;
     const float4 a = __ldcs(reinterpret_cast<const float4*>(in + e0));
     const float4 b = __ldcs(reinterpret_cast<const float4*>(in + e1));
-    uint32_t pa[kGroup], pb[kGroup];
-    noise_pos4(goff + e0, pa);
-    noise_pos4(goff + e1, pb);
     uint2 qa, qb;
-    qa.x = pack_hi16(sr_bf16_hi(a.x, draw16_complement(pa[0], seed)), sr_bf16_hi(a.y, draw16_complement(pa[1], seed)));
-    qa.y = pack_hi16(sr_bf16_hi(a.z, draw16_complement(pa[2], seed)), sr_bf16_hi(a.w, draw16_complement(pa[3], seed)));
-    qb.x = pack_hi16(sr_bf16_hi(b.x, draw16_complement(pb[0], seed)), sr_bf16_hi(b.y, draw16_complement(pb[1], seed)));
-    qb.y = pack_hi16(sr_bf16_hi(b.z, draw16_complement(pb[2], seed)), sr_bf16_hi(b.w, draw16_complement(pb[3], seed)));
+    sr_pack8(a, b, goff + e0, goff + e1, seed, qa, qb);
     __stcs(reinterpret_cast<uint2*>(out + e0), qa);
     __stcs(reinterpret_cast<uint2*>(out + e1), qb);
   }
@@ -126,15 +121,15 @@ sr_fp16_vec_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uin
     const float4 a = __ldcs(reinterpret_cast<const float4*>(in + e0));
     const float4 b = __ldcs(reinterpret_cast<const float4*>(in + e1));
     uint32_t pa[kGroup], pb[kGroup];
-    noise_pos4(goff + e0, pa);
-    noise_pos4(goff + e1, pb);
+    noise_first4(goff + e0, seed, pa);
+    noise_first4(goff + e1, seed, pb);
     // Per group set (a: groups 4t, b: groups 4t + 1024): a warp whose 128
     // elements all lie in fp16's normal range takes the short form; the
     // vote keeps the warp converged.
     const bool na = fp16_normal_range(a.x) & fp16_normal_range(a.y) & fp16_normal_range(a.z) & fp16_normal_range(a.w);
     const bool nb = fp16_normal_range(b.x) & fp16_normal_range(b.y) & fp16_normal_range(b.z) & fp16_normal_range(b.w);
-    const uint2 qa = __all_sync(0xFFFFFFFFu, na) ? sr_fp16_pack4<true>(a, pa, seed) : sr_fp16_pack4<false>(a, pa, seed);
-    const uint2 qb = __all_sync(0xFFFFFFFFu, nb) ? sr_fp16_pack4<true>(b, pb, seed) : sr_fp16_pack4<false>(b, pb, seed);
+    const uint2 qa = __all_sync(0xFFFFFFFFu, na) ? sr_fp16_pack4<true>(a, pa) : sr_fp16_pack4<false>(a, pa);
+    const uint2 qb = __all_sync(0xFFFFFFFFu, nb) ? sr_fp16_pack4<true>(b, pb) : sr_fp16_pack4<false>(b, pb);
     __stcs(reinterpret_cast<uint2*>(out + e0), qa);
     __stcs(reinterpret_cast<uint2*>(out + e1), qb);
   }
@@ -154,7 +149,7 @@ sr_fp16_scalar_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, 
 
 // acc[i] = SR((float)acc[i] + delta[i], goff + i, seed), in place. Vector
 // path: acc 8-B aligned, delta 16-B aligned; the step's tiling.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kSrBlocksPerSm)
 accumulate_vec_kernel(uint16_t* __restrict__ acc, const float* __restrict__ delta, uint64_t goff, uint64_t n,
                       uint32_t seed) {
   pdl_enter();
@@ -166,18 +161,12 @@ accumulate_vec_kernel(uint16_t* __restrict__ acc, const float* __restrict__ delt
     const uint2 a1 = __ldcs(reinterpret_cast<const uint2*>(acc + e1));
     const float4 d0 = __ldcs(reinterpret_cast<const float4*>(delta + e0));
     const float4 d1 = __ldcs(reinterpret_cast<const float4*>(delta + e1));
-    uint32_t p0[kGroup], p1[kGroup];
-    noise_pos4(goff + e0, p0);
-    noise_pos4(goff + e1, p1);
+    const float4 s0 = make_float4(__fadd_rn(bf16_lo(a0.x), d0.x), __fadd_rn(bf16_hi(a0.x), d0.y),
+                                  __fadd_rn(bf16_lo(a0.y), d0.z), __fadd_rn(bf16_hi(a0.y), d0.w));
+    const float4 s1 = make_float4(__fadd_rn(bf16_lo(a1.x), d1.x), __fadd_rn(bf16_hi(a1.x), d1.y),
+                                  __fadd_rn(bf16_lo(a1.y), d1.z), __fadd_rn(bf16_hi(a1.y), d1.w));
     uint2 q0, q1;
-    q0.x = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a0.x), d0.x), draw16_complement(p0[0], seed)),
-                     sr_bf16_hi(__fadd_rn(bf16_hi(a0.x), d0.y), draw16_complement(p0[1], seed)));
-    q0.y = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a0.y), d0.z), draw16_complement(p0[2], seed)),
-                     sr_bf16_hi(__fadd_rn(bf16_hi(a0.y), d0.w), draw16_complement(p0[3], seed)));
-    q1.x = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a1.x), d1.x), draw16_complement(p1[0], seed)),
-                     sr_bf16_hi(__fadd_rn(bf16_hi(a1.x), d1.y), draw16_complement(p1[1], seed)));
-    q1.y = pack_hi16(sr_bf16_hi(__fadd_rn(bf16_lo(a1.y), d1.z), draw16_complement(p1[2], seed)),
-                     sr_bf16_hi(__fadd_rn(bf16_hi(a1.y), d1.w), draw16_complement(p1[3], seed)));
+    sr_pack8(s0, s1, goff + e0, goff + e1, seed, q0, q1);
     __stcs(reinterpret_cast<uint2*>(acc + e0), q0);
     __stcs(reinterpret_cast<uint2*>(acc + e1), q1);
   }
