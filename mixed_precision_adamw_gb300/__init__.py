@@ -580,11 +580,57 @@ class Optimizer:
             raise MpError(st, "mp_adamw_step (device)")
 
 
+class HostGradPipeline:
+    """Optimizer steps whose gradients arrive in page-locked host memory,
+    with each step's host-to-device copy overlapped with the previous step's
+    update.
+
+    Two device gradient buffers alternate: step t's copy (a copy engine, on
+    its own stream) fills buffer t % 2 while the compute stream still runs
+    step t - 1 on the other one; the step waits for its copy (an event), and
+    a copy waits for the step that last read its buffer. Every step is one
+    Optimizer.step call (mp_optimizer_step) on the compute stream; the norm
+    can be copied back to a page-locked host float each step. Nothing here
+    synchronises the host.
+    """
+
+    def __init__(self, opt: "Optimizer", device=None):
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.opt = opt
+        self.buffers = [torch.empty(opt.n, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.used = [None, None]  # event after the last step that read each buffer
+        self.k = 0
+
+    def step(self, params, host_grads: torch.Tensor, master, m, v, t: int, seed: int, host_norm=None,
+             stream=None):
+        if host_grads.is_cuda or not host_grads.is_pinned():
+            raise ValueError("host_grads: page-locked host memory expected")
+        compute = stream if stream is not None else torch.cuda.current_stream(self.buffers[0].device)
+        b = self.k % 2
+        self.k += 1
+        buf = self.buffers[b]
+        with torch.cuda.stream(self.copy_stream):
+            if self.used[b] is not None:
+                self.copy_stream.wait_event(self.used[b])
+            buf.copy_(host_grads.view(buf.dtype), non_blocking=True)
+            self.copied[b].record(self.copy_stream)
+        compute.wait_event(self.copied[b])
+        self.opt.step(params, buf, master, m, v, t, seed, stream=compute)
+        if host_norm is not None:
+            with torch.cuda.stream(compute):
+                host_norm.copy_(self.opt.d_norm, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(compute)
+        self.used[b] = ev
+
+
 __all__ = [
     "MpError", "MpTensor", "MpHyper", "TensorTable", "Optimizer", "OutlierDetector", "lib", "abi_version",
     "status_string", "last_cuda_error", "mp_grad_norm_workspace_bytes", "mp_grad_norm", "mp_grad_norm_noalloc",
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
     "mp_stochastic_round", "mp_stochastic_round_fp16", "mp_accumulate_sr", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
     "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH", "mp_grad_sumsq", "mp_clip_scale_from_sumsq",
-    "LRSchedule", "MpLrSchedule", "LR_KINDS",
+    "LRSchedule", "MpLrSchedule", "LR_KINDS", "HostGradPipeline",
 ]

@@ -40,6 +40,10 @@ struct StepArgs {
   uint32_t seed;
   uint32_t nseg;         // segments covering [goff, goff + n)
   uint32_t first_decay;  // decay flag of segment 0; flags alternate after it
+  // Vector path: elements [0, head) go one per thread and the tiles start at
+  // element head, chosen so that the tiles' gradient and weight vectors
+  // start on 128-B lines (a multiple of 4 below 64; 0 elsewhere).
+  uint32_t head;
   // Non-null: lr, bc1, bc2 and seed are read from this device state (written
   // by the norm's finalize kernel earlier in the stream) instead of the
   // fields above.

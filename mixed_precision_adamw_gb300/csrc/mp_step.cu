@@ -28,8 +28,10 @@ struct VecOccupancy {
   static constexpr int kMinBlocks = kMaster ? 3 : 4;
 };
 
-// Vector path: the tiles of this block (vec_tiles in mp_step.cuh).
-template <bool kMaster, uint32_t CAP, bool kDev>
+// Vector path: the tiles of this block (vec_tiles in mp_step.cuh). kHead:
+// the range starts mid-line and a head is peeled first (a separate
+// instantiation, so that aligned ranges run the plain tile loop).
+template <bool kMaster, uint32_t CAP, bool kDev, bool kHead>
 __global__ void __launch_bounds__(kThreads, VecOccupancy<kMaster>::kMinBlocks)
 adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ SegTable<CAP> segs) {
   pdl_enter();
@@ -37,7 +39,7 @@ adamw_vec_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ Seg
   if (!read_scale(p, scale)) return;
   uint32_t seed;
   const Hyper h = step_scalars<kDev>(p, seed);
-  vec_tiles<kMaster>(p, segs, scale, h, seed, blockIdx.x, gridDim.x);
+  vec_tiles<kMaster, kHead>(p, segs, scale, h, seed, blockIdx.x, gridDim.x);
 }
 
 // Scalar path for buffers that are not vector-aligned: same arithmetic.
@@ -80,15 +82,25 @@ cudaError_t launch_cap(const StepArgs& a, const uint64_t* seg_end, bool vec, con
   SegTable<CAP> t;
   for (uint32_t s = 0; s < a.nseg; ++s) t.end[s] = seg_end[s];
   for (uint32_t s = a.nseg; s < CAP; ++s) t.end[s] = seg_end[a.nseg - 1];
-  static std::atomic<int> vec_occupancy[64], scalar_occupancy[64];  // one cache per <kMaster, CAP, kDev> kernel
-  const uint64_t ntiles = a.n / kTile;
+  // one cache per kernel: <kMaster, CAP, kDev> and the vector kernel's kHead
+  static std::atomic<int> vec_occupancy[64], vec_head_occupancy[64], scalar_occupancy[64];
   if (vec) {
-    auto k = adamw_vec_kernel<kMaster, CAP, kDev>;
-    const uint64_t cap = static_cast<uint64_t>(dev.sms) * blocks_per_sm(k, dev.device, vec_occupancy);
-    uint64_t blocks = ntiles ? ntiles : (a.n + kThreads - 1) / kThreads;
+    // Peel the elements before the gradients' next 128-B line (a multiple of
+    // 4 below 64, as grads are 8-B aligned), so that the tiles' vectors start
+    // on whole lines: a range that starts mid-line (a shard of a size that
+    // is not a multiple of 64) would otherwise split every warp's accesses
+    // across an extra line.
+    StepArgs b = a;
+    const uint32_t head = static_cast<uint32_t>(((128u - (reinterpret_cast<uintptr_t>(a.grads) & 127u)) & 127u) / 2u);
+    b.head = static_cast<uint64_t>(head) < a.n ? head : static_cast<uint32_t>(a.n);
+    const uint64_t ntiles = (b.n - b.head) / kTile;
+    auto k = b.head ? adamw_vec_kernel<kMaster, CAP, kDev, true> : adamw_vec_kernel<kMaster, CAP, kDev, false>;
+    const uint64_t cap = static_cast<uint64_t>(dev.sms) *
+                         blocks_per_sm(k, dev.device, b.head ? vec_head_occupancy : vec_occupancy);
+    uint64_t blocks = ntiles ? ntiles : (b.n + kThreads - 1) / kThreads;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(k, static_cast<unsigned>(blocks), kThreads, stream, a, t);
+    return launch_pdl(k, static_cast<unsigned>(blocks), kThreads, stream, b, t);
   } else {
     auto k = adamw_scalar_kernel<kMaster, CAP, kDev>;
     const uint64_t cap = static_cast<uint64_t>(dev.sms) * blocks_per_sm(k, dev.device, scalar_occupancy);

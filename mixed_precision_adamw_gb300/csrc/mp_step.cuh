@@ -210,26 +210,34 @@ __device__ __forceinline__ void update_tile(const StepArgs& p, const SegTable<CA
 
 // The vector path's tiles for block `block` of `nblocks` (the mapping of a
 // grid of nblocks blocks). Requires params/grads 8-B aligned and master/m/v
-// 16-B aligned. Block-iteration k covers tile k of kTile elements; thread t
-// handles the two 4-element groups at tile offsets 4t and 4t + 4*kThreads, so
-// every warp-wide load or store is one contiguous 512-B (fp32) or 256-B
-// (bf16) span; the ragged tail (< kTile elements) goes one element per
-// thread.
-template <bool kMaster, uint32_t CAP>
+// 16-B aligned. The first p.head elements (a multiple of 4, below 64) go one
+// per thread; then block-iteration k covers tile k of kTile elements from
+// element p.head; thread t handles the two 4-element groups at tile offsets
+// 4t and 4t + 4*kThreads, so every warp-wide load or store is one contiguous
+// 512-B (fp32) or 256-B (bf16) span, which starts on a 128-B line when the
+// arrays' starts agree modulo 128 B (the head is chosen for that); the
+// ragged tail (< kTile elements) goes one element per thread.
+// kHead false compiles the peel away (p.head must then be 0).
+template <bool kMaster, bool kHead, uint32_t CAP>
 __device__ __forceinline__ void vec_tiles(const StepArgs& p, const SegTable<CAP>& segs, float scale,
                                           const Hyper& h, uint32_t seed, uint32_t block, uint32_t nblocks) {
-  const uint64_t ntiles = p.n / kTile;
+  const uint64_t head = kHead ? (p.head < p.n ? p.head : p.n) : 0;
+  const uint64_t ntiles = (p.n - head) / kTile;
   const uint64_t stride_tail = static_cast<uint64_t>(nblocks) * kThreads;
-  const uint64_t tail0 = ntiles * kTile + static_cast<uint64_t>(block) * kThreads + threadIdx.x;
-  uint64_t first = (block < ntiles) ? static_cast<uint64_t>(block) * kTile + threadIdx.x * kGroup
-                                         : tail0;
+  const uint64_t lane0 = static_cast<uint64_t>(block) * kThreads + threadIdx.x;
+  const uint64_t tail0 = head + ntiles * kTile + lane0;
+  uint64_t first = lane0 < head ? lane0
+                 : (block < ntiles) ? head + static_cast<uint64_t>(block) * kTile + threadIdx.x * kGroup
+                                    : tail0;
   if (first >= p.n) first = p.n - 1;
   Cursor c;
   c.s = seg_find(segs, p.nseg, p.goff + first);
   c.end = segs.end[c.s];
 
+  // Head (< 64 elements), one element per thread: indices below every tile's.
+  for (uint64_t i = lane0; i < head; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
   for (uint64_t tile = block; tile < ntiles; tile += nblocks) {
-    const uint64_t e0 = tile * kTile + threadIdx.x * kGroup;
+    const uint64_t e0 = head + tile * kTile + threadIdx.x * kGroup;
     TileIn in;
     load_tile<kMaster>(p, p.grads, e0, in);
     update_tile<kMaster>(p, segs, c, e0, in, scale, h, seed);

@@ -152,3 +152,39 @@ def test_host_gradients_extreme_values_take_the_fp64_path(scale):
     assert opt_a.d_norm.item() == opt_b.d_norm.item() and np.isfinite(opt_a.d_norm.item())
     for k in a:
         assert _same(a[k], b[k]), k
+
+
+def test_host_gradient_pipeline_equals_device_gradient_steps():
+    """HostGradPipeline: each step's gradients copied from page-locked host
+    memory on a copy stream, overlapped with the previous step's update; 6
+    steps with different gradients must equal the same steps on device
+    gradients bit for bit, and the host norms must be each step's norm."""
+    tab, st, _ = _setup()
+    H = W.HYPER
+    kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
+    n = st["m"].numel()
+    entries_n = n
+    a = {k: x.clone() for k, x in st.items()}
+    b = {k: x.clone() for k, x in st.items()}
+    grads = [(torch.randn(entries_n, device="cuda", generator=torch.Generator(device="cuda").manual_seed(s))
+              * 1e-2 * (1 + s)).to(torch.bfloat16) for s in range(6)]
+    host = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(6)]
+    for h, g in zip(host, grads):
+        h.copy_(g)
+    norms = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(6)]
+    opt_a = mp.Optimizer(tab, clip=H["clip"], **kw)
+    pipe = mp.HostGradPipeline(opt_a)
+    for t in range(1, 7):
+        pipe.step(a["params"], host[t - 1], a["master"], a["m"], a["v"], t, W.step_seed(t), host_norm=norms[t - 1])
+    opt_b = mp.Optimizer(tab, clip=H["clip"], **kw)
+    ref_norms = []
+    for t in range(1, 7):
+        opt_b.step(b["params"], grads[t - 1], b["master"], b["m"], b["v"], t, W.step_seed(t))
+        ref_norms.append(opt_b.d_norm.clone())
+    torch.cuda.synchronize()
+    for k in a:
+        assert _same(a[k], b[k]), k
+    for got, ref in zip(norms, ref_norms):
+        assert float(got.item()) == float(ref.item())
+    with pytest.raises(ValueError):
+        pipe.step(a["params"], grads[0], a["master"], a["m"], a["v"], 7, 7)  # device tensor, not pinned host

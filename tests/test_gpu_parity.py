@@ -443,6 +443,27 @@ def test_step_random_tables(n, pad, with_master, tmax):
     _compare(d, host, f"random n={n}")
 
 
+@pytest.mark.parametrize("with_master", [True, False])
+def test_step_every_line_offset_of_the_vector_path(with_master):
+    """Buffers that start 4k elements past a 128-B line (k = 0 .. 15): the
+    vector kernel peels the elements before the gradients' next line one per
+    thread and tiles the rest; every offset must give the oracle's bits."""
+    n = 2048 * 5 + 77
+    tab, params, grads, master, m, v = _random_case(n, 4242, 1, 300)
+    lr, b1, b2, eps, wd, scale, t, seed = 2e-3, 0.9, 0.95, 1e-8, 0.1, 0.81, 3, 5
+    host = dict(params=params.copy(), master=master.copy() if with_master else None, m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], 0, tab, lr, b1, b2, eps,
+                             wd, f32(scale), t, seed) == 0
+    d_scale = torch.tensor([scale], dtype=torch.float32, device=DEV)
+    for k in range(16):
+        pad = 4 * k
+        d = dict(params=dev_u16(params, pad), grads=dev_u16(grads, pad), m=dev_f32(m, pad), v=dev_f32(v, pad),
+                 master=dev_f32(master, pad) if with_master else None)
+        mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=lr,
+                         beta1=b1, beta2=b2, eps=eps, weight_decay=wd, d_grad_scale=d_scale, t=t, seed=seed)
+        _compare(d, host, f"line offset {pad} elements")
+
+
 @pytest.mark.parametrize("goff", [(1 << 32) - 3001, (1 << 32) - 3002, (1 << 32) - 3003, (1 << 32) - 3004])
 def test_step_global_offset_across_2_pow_32(goff):
     """A shard whose global range crosses index 2^32 from an offset that is
