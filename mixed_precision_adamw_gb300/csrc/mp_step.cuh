@@ -226,16 +226,19 @@ __device__ __forceinline__ void vec_tiles(const StepArgs& p, const SegTable<CAP>
   const uint64_t stride_tail = static_cast<uint64_t>(nblocks) * kThreads;
   const uint64_t lane0 = static_cast<uint64_t>(block) * kThreads + threadIdx.x;
   const uint64_t tail0 = head + ntiles * kTile + lane0;
-  uint64_t first = lane0 < head ? lane0
-                 : (block < ntiles) ? head + static_cast<uint64_t>(block) * kTile + threadIdx.x * kGroup
-                                    : tail0;
+  uint64_t first = (block < ntiles) ? head + static_cast<uint64_t>(block) * kTile + threadIdx.x * kGroup : tail0;
+  if constexpr (kHead) {
+    if (lane0 < head) first = lane0;
+  }
   if (first >= p.n) first = p.n - 1;
   Cursor c;
   c.s = seg_find(segs, p.nseg, p.goff + first);
   c.end = segs.end[c.s];
 
   // Head (< 64 elements), one element per thread: indices below every tile's.
-  for (uint64_t i = lane0; i < head; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
+  if constexpr (kHead) {
+    for (uint64_t i = lane0; i < head; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
+  }
   for (uint64_t tile = block; tile < ntiles; tile += nblocks) {
     const uint64_t e0 = head + tile * kTile + threadIdx.x * kGroup;
     TileIn in;
