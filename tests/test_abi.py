@@ -270,3 +270,65 @@ def test_step_launch_plan_checks(mp):
     assert L.mp_step_launches(0, 101, tab.ctypes_array, 1, None, 0, C.byref(cnt)) == mp.MP_ERR_TABLE
     assert L.mp_step_launches(0, 100, None, 1, None, 0, C.byref(cnt)) == mp.MP_ERR_NULL
     assert L.mp_step_launches(0, 100, tab.ctypes_array, 1, None, 0, C.byref(cnt)) == mp.MP_OK and cnt.value == 1
+
+
+def test_split_norm_argument_checks(mp):
+    """mp_grad_sumsq and mp_clip_scale_from_sumsq reject bad input before any
+    device work (the ZeRO-1 norm's two halves)."""
+    L = mp.lib()
+    assert L.mp_grad_sumsq(None, 10, FAKE, 4096, FAKE, None) == mp.MP_ERR_NULL
+    assert L.mp_grad_sumsq(FAKE, 10, FAKE, 4096, None, None) == mp.MP_ERR_NULL
+    assert L.mp_grad_sumsq(FAKE, 10, None, 4096, FAKE, None) == mp.MP_ERR_WORKSPACE
+    assert L.mp_grad_sumsq(FAKE + 1, 10, FAKE, 4096, FAKE, None) == mp.MP_ERR_ALIGN
+    assert L.mp_grad_sumsq(FAKE, 10, FAKE + 4, 4096, FAKE, None) == mp.MP_ERR_ALIGN
+    assert L.mp_grad_sumsq(FAKE, 10, FAKE, 4096, FAKE + 4, None) == mp.MP_ERR_ALIGN
+    assert L.mp_grad_sumsq(FAKE, (1 << 62) + 1, FAKE, 4096, FAKE, None) == mp.MP_ERR_RANGE
+    assert L.mp_clip_scale_from_sumsq(None, 2, 1.0, FAKE, FAKE, None, None) == mp.MP_ERR_NULL
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, 1.0, None, FAKE, None, None) == mp.MP_ERR_NULL
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, 1.0, FAKE, None, None, None) == mp.MP_ERR_NULL
+    assert L.mp_clip_scale_from_sumsq(FAKE + 4, 2, 1.0, FAKE, FAKE, None, None) == mp.MP_ERR_ALIGN
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, 1.0, FAKE + 2, FAKE, None, None) == mp.MP_ERR_ALIGN
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, 1.0, FAKE, FAKE, FAKE + 4, None) == mp.MP_ERR_ALIGN
+    assert L.mp_clip_scale_from_sumsq(FAKE, 0, 1.0, FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+    assert L.mp_clip_scale_from_sumsq(FAKE, (1 << 20) + 1, 1.0, FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, 0.0, FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+    assert L.mp_clip_scale_from_sumsq(FAKE, 2, float("nan"), FAKE, FAKE, None, None) == mp.MP_ERR_RANGE
+
+
+@pytest.mark.parametrize("kind", ["constant", "cosine", "linear", "wsd"])
+def test_lr_schedule_matches_the_oracle(mp, kind):
+    """mp_lr_at (host only) against the oracle's schedule, bit for bit, over
+    warm-up, decay and past the end, for several shapes of run."""
+    import oracle
+    for warmup, total, hi, lo, f in ((0, 1, 3e-4, 0.0, 1.0), (10, 110, 6e-4, 6e-5, 0.2), (2000, 60000, 1e-3, 1e-5, 0.1),
+                                     (7, 13, 0.5, 0.25, 0.5)):
+        s = mp.LRSchedule(kind, lr_max=hi, lr_min=lo, warmup=warmup, total=total, decay_frac=f)
+        for t in list(range(1, min(total, 400) + 3)) + [total - 1, total, total + 1, 10 * total + 5]:
+            if t < 1:
+                continue
+            ref = oracle.lr(mp.LR_KINDS[kind], warmup, total, hi, lo, f, t)
+            assert s.lr(t) == float(ref), (kind, warmup, total, t)
+
+
+def test_lr_schedule_checks(mp):
+    L = mp.lib()
+    out = ctypes.c_float()
+
+    def call(kind, warmup, total, hi, lo, f, t, reserved=0):
+        s = mp.MpLrSchedule(kind, reserved, warmup, total, hi, lo, f, 0.0)
+        return L.mp_lr_at(ctypes.byref(s), t, ctypes.byref(out))
+
+    assert L.mp_lr_at(None, 1, ctypes.byref(out)) == mp.MP_ERR_NULL
+    assert call(1, 10, 100, 1e-3, 0.0, 0.0, 0) == mp.MP_ERR_RANGE        # t < 1
+    assert call(4, 10, 100, 1e-3, 0.0, 0.0, 5) == mp.MP_ERR_RANGE        # unknown kind
+    assert call(1, 100, 100, 1e-3, 0.0, 0.0, 5) == mp.MP_ERR_RANGE       # total <= warmup
+    assert call(1, -1, 100, 1e-3, 0.0, 0.0, 5) == mp.MP_ERR_RANGE        # negative warm-up
+    assert call(3, 10, 100, 1e-3, 0.0, 0.0, 5) == mp.MP_ERR_RANGE        # WSD without a decay fraction
+    assert call(3, 10, 100, 1e-3, 0.0, 1.5, 5) == mp.MP_ERR_RANGE
+    assert call(1, 10, 100, float("inf"), 0.0, 0.0, 5) == mp.MP_ERR_RANGE
+    assert call(1, 10, 100, 1e-3, 0.0, 0.0, 5, reserved=1) == mp.MP_ERR_RANGE
+    assert call(0, 0, 0, 1e-3, 0.0, 0.0, 5) == mp.MP_OK and out.value == np.float32(1e-3)  # constant needs no total
+    with pytest.raises(ValueError):
+        mp.LRSchedule("step", lr_max=1e-3)
+    with pytest.raises(mp.MpError):
+        mp.LRSchedule("cosine", lr_max=1e-3, warmup=5, total=5)
