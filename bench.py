@@ -926,10 +926,18 @@ def main(argv=None):
         line = run_zero1(args, world, rank, local)
     else:
         line = run_ours(args, world, rank, local)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    # anything a native library wrote to C stdio (e.g. NCCL's version line)
+    # goes out before the JSON line, which stays the last line on stdout
+    sys.stdout.flush()
+    try:
+        import ctypes
+        ctypes.CDLL(None).fflush(None)
+    except (OSError, AttributeError):
+        pass
     if line is not None:
         print(json.dumps(line), flush=True)
-    if world > 1 and torch.distributed.is_initialized():
-        torch.distributed.destroy_process_group()
 
 
 if __name__ == "__main__":
