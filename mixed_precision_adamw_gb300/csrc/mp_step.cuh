@@ -103,6 +103,19 @@ __device__ __forceinline__ uint2 group_update(uint2 graw, float4& m4, float4& v4
   return make_uint2(pack_hi16(r[0], r[1]), pack_hi16(r[2], r[3]));
 }
 
+// Updates 4 consecutive elements: m, v and the new fp32 weights w (the
+// rounding is left to the caller).
+__device__ __forceinline__ void group_update_only(uint2 graw, float4& m4, float4& v4, float (&w)[kGroup],
+                                                  const float (&wd)[kGroup], float scale, const Hyper& h) {
+  const float g[kGroup] = {bf16_lo(graw.x), bf16_hi(graw.x), bf16_lo(graw.y), bf16_hi(graw.y)};
+  float mm[kGroup] = {m4.x, m4.y, m4.z, m4.w};
+  float vv[kGroup] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+  for (int j = 0; j < kGroup; ++j) w[j] = adamw_update(g[j], mm[j], vv[j], w[j], wd[j], scale, h);
+  m4 = make_float4(mm[0], mm[1], mm[2], mm[3]);
+  v4 = make_float4(vv[0], vv[1], vv[2], vv[3]);
+}
+
 // One element's inputs: its gradient, m, v and old weight.
 struct ElemIn {
   float g, m, v, old;
@@ -193,8 +206,16 @@ __device__ __forceinline__ void update_tile(const StepArgs& p, const SegTable<CA
   group_decay(c, segs, p, p.goff + e0, wd0);
   group_decay(c, segs, p, p.goff + e1, wd1);
 
-  const uint2 q0 = group_update(in.g0, in.m0, in.v0, in.w0, wd0, scale, h, p.goff + e0, seed);
-  const uint2 q1 = group_update(in.g1, in.m1, in.v1, in.w1, wd1, scale, h, p.goff + e1, seed);
+  uint2 q0, q1;
+  if constexpr (kMaster) {
+    q0 = group_update(in.g0, in.m0, in.v0, in.w0, wd0, scale, h, p.goff + e0, seed);
+    q1 = group_update(in.g1, in.m1, in.v1, in.w1, wd1, scale, h, p.goff + e1, seed);
+  } else {
+    group_update_only(in.g0, in.m0, in.v0, in.w0, wd0, scale, h);
+    group_update_only(in.g1, in.m1, in.v1, in.w1, wd1, scale, h);
+    sr_pack8(make_float4(in.w0[0], in.w0[1], in.w0[2], in.w0[3]), make_float4(in.w1[0], in.w1[1], in.w1[2], in.w1[3]),
+             p.goff + e0, p.goff + e1, seed, q0, q1);
+  }
 
   __stcs(reinterpret_cast<float4*>(p.m + e0), in.m0);
   __stcs(reinterpret_cast<float4*>(p.m + e1), in.m1);
