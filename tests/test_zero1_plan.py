@@ -1,4 +1,5 @@
-"""The ZeRO-1 step's collective plan on CPU ranks (gloo, world size 2).
+"""The ZeRO-1 step on CPU ranks (gloo, world size 2): its collective plan,
+and its results against plain data parallelism.
 
 llm.c walk-through ch. 04 §3.2-§3.3 and §4: a reduce-scatter (average) of
 the full gradients, each rank's sum of squares of its own shard, those sums
@@ -6,7 +7,9 @@ combined across ranks, the shard update at its global offset, an all-gather
 of the new bf16 weights. Here the library's kernels are replaced by stubs
 that only record their arguments and write tags (none of the optimizer's
 arithmetic), and the collectives are real gloo collectives; the test checks
-what each rank received and sent.
+what each rank received and sent. A second test puts the oracle's arithmetic
+behind the same calls and requires ZeRO-1 to give data parallelism's weights
+and state bit for bit (CMU 11-667 lecture 13 notes §5.2: max difference 0).
 """
 import os
 import socket
@@ -112,3 +115,101 @@ def test_shard_layout_rules():
         ShardLayout(10, 3, 0)  # must divide (llm.c ch. 04 §3.2)
     with pytest.raises(ValueError):
         ShardLayout(12, 3, 3)
+
+
+class OracleKernels:
+    """The oracle's arithmetic behind the ZeRO-1 driver's three kernel calls,
+    on CPU tensors (test-only: it checks the driver's plumbing with real
+    arithmetic, not the CUDA kernels)."""
+
+    def __init__(self):
+        import oracle
+        self.o = oracle
+
+    def workspace_bytes(self, n):
+        return 64
+
+    @staticmethod
+    def _u16(t):
+        import numpy as np
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    def grad_sumsq(self, grads, workspace, d_sumsq, n=None, stream=None):
+        d_sumsq.fill_(self.o.sumsq(self._u16(grads)))
+
+    def clip_scale_from_sumsq(self, d_sumsq, clip, d_norm, d_scale, count=None, stream=None):
+        _, nrm, sc = self.o.norm_from_parts(d_sumsq.numpy(), clip)
+        d_norm.fill_(float(nrm))
+        d_scale.fill_(float(sc))
+
+    def adamw_step(self, params, grads, master, m, v, table, *, d_grad_scale, t, seed, global_offset, n,
+                   d_status, stream, lr, beta1, beta2, eps, weight_decay):
+        entries = [(table.ctypes_array[i].offset, table.ctypes_array[i].size, table.ctypes_array[i].decay)
+                   for i in range(table.n_tensors)]
+        st = self.o.adamw_step(self._u16(params), self._u16(grads), master.numpy() if master is not None else None,
+                               m.numpy(), v.numpy(), global_offset, entries, lr, beta1, beta2, eps, weight_decay,
+                               float(d_grad_scale.item()), t, seed)
+        assert st == 0
+
+
+def _pow2_grads(rank, step, n):
+    """+-2^k gradients (k in [-12, -5]): the two ranks' average (the
+    collective's own bf16 arithmetic, the same in the reduce-scatter and the
+    all-reduce) has few significant bits and a narrow range, so every sum of
+    its squares is exact in fp64 and the ZeRO-1 and data-parallel norms
+    agree exactly."""
+    g = torch.Generator().manual_seed(1000 * step + rank)
+    k = torch.randint(-12, -4, (n,), generator=g).float()
+    s = torch.where(torch.rand(n, generator=g) < 0.5, -1.0, 1.0)
+    return (s * torch.exp2(k)).to(torch.bfloat16)
+
+
+def _dp_worker(rank, world, port, q):
+    """Three steps of ZeRO-1 (the driver, oracle arithmetic) and of plain data
+    parallelism (all-reduce average, every rank the whole buffer) from the
+    same state: the weights must agree bit for bit (CMU 11-667 lecture 13
+    notes §5.2: maximum difference 0)."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle
+        from mixed_precision_adamw_gb300.zero1 import Zero1Optimizer
+        H = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+        gen = torch.Generator().manual_seed(5)
+        master0 = torch.randn(N, generator=gen) * 0.02
+        zopt = Zero1Optimizer(TABLE, clip=1.0, device="cpu", kernels=OracleKernels(), **H)
+        z = zopt.make_shard_state(master0)
+        z_params = master0.to(torch.bfloat16)
+        d_params, d_master = master0.to(torch.bfloat16), master0.clone()
+        d_m, d_v = torch.zeros(N), torch.zeros(N)
+        u16 = OracleKernels._u16
+        for t in (1, 2, 3):
+            g = _pow2_grads(rank, t, N)
+            zopt.step(z_params, g.clone(), z["master"], z["m"], z["v"], t=t, seed=100 + t)
+            avg = g.clone()
+            dist.all_reduce(avg, op=dist.ReduceOp.AVG)
+            _, _, sc = oracle.grad_norm(u16(avg), 1.0)
+            assert oracle.adamw_step(u16(d_params), u16(avg), d_master.numpy(), d_m.numpy(), d_v.numpy(), 0, TABLE,
+                                     H["lr"], H["beta1"], H["beta2"], H["eps"], H["weight_decay"], float(sc), t,
+                                     100 + t) == 0
+        sl = zopt.layout.slice()
+        q.put((rank, torch.equal(z_params.view(torch.int16), d_params.view(torch.int16)),
+               torch.equal(z["master"], d_master[sl]), torch.equal(z["m"], d_m[sl]), torch.equal(z["v"], d_v[sl])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_zero1_equals_data_parallel_bit_for_bit_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mproc.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = sorted(q.get(timeout=300) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, params_eq, master_eq, m_eq, v_eq in out:
+        assert params_eq and master_eq and m_eq and v_eq, (rank, params_eq, master_eq, m_eq, v_eq)
