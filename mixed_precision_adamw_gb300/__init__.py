@@ -591,7 +591,8 @@ class HostGradPipeline:
     a copy waits for the step that last read its buffer. Every step is one
     Optimizer.step call (mp_optimizer_step) on the compute stream; the norm
     can be copied back to a page-locked host float each step. Nothing here
-    synchronises the host.
+    synchronises the host, so a host buffer passed to step() must not be
+    rewritten before its copy has run: wait on last_copy() (an event) first.
     """
 
     def __init__(self, opt: "Optimizer", device=None):
@@ -624,6 +625,12 @@ class HostGradPipeline:
         ev = torch.cuda.Event()
         ev.record(compute)
         self.used[b] = ev
+
+    def last_copy(self) -> torch.cuda.Event:
+        """The event recorded after the latest step's host-to-device copy: once
+        it has completed (.synchronize() or .query()), that host buffer may be
+        rewritten."""
+        return self.copied[(self.k - 1) % 2]
 
 
 __all__ = [

@@ -186,5 +186,20 @@ def test_host_gradient_pipeline_equals_device_gradient_steps():
         assert _same(a[k], b[k]), k
     for got, ref in zip(norms, ref_norms):
         assert float(got.item()) == float(ref.item())
+    # one host buffer reused for every step, rewritten after each copy has run
+    c = {k: x.clone() for k, x in a.items()}
+    d = {k: x.clone() for k, x in a.items()}
+    opt_c = mp.Optimizer(tab, clip=H["clip"], **kw)
+    opt_d = mp.Optimizer(tab, clip=H["clip"], **kw)
+    pipe_c = mp.HostGradPipeline(opt_c)
+    one = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    for t in range(7, 10):
+        pipe_c.last_copy().synchronize()
+        one.copy_(grads[t - 7])
+        pipe_c.step(c["params"], one, c["master"], c["m"], c["v"], t, W.step_seed(t))
+        opt_d.step(d["params"], grads[t - 7], d["master"], d["m"], d["v"], t, W.step_seed(t))
+    torch.cuda.synchronize()
+    for k in c:
+        assert _same(c[k], d[k]), k
     with pytest.raises(ValueError):
         pipe.step(a["params"], grads[0], a["master"], a["m"], a["v"], 7, 7)  # device tensor, not pinned host
