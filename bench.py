@@ -682,11 +682,12 @@ def measure_sr_stress(mp, stream, device, peak, n=64 << 20, steps=1000):
 def measure_e2e(mp, st, g, opt, N, stream, device, kw, iters, step_no):
     """Through the public API with host buffers: every step's bf16 gradients
     are copied from pinned host memory and the norm is read back to pinned
-    host memory. Main figure: HostGradPipeline (a copy engine moves step t's
-    gradients while the GPU updates step t - 1; one mp_optimizer_step call
-    per step). Also reported: the same steps as single mp_optimizer_step
-    calls whose norm kernel reads the host gradients over the link itself
-    (no overlap across steps)."""
+    host memory. Main figure: HostGradPipeline (the SMs copy step t's
+    gradients, one block per SM, while the GPU updates step t - 1; one
+    mp_optimizer_step call per step). Also reported: the same pipeline with a
+    copy engine moving the gradients, and single mp_optimizer_step calls
+    whose norm kernel reads the host gradients over the link itself (no
+    overlap across steps)."""
     host_g = torch.empty(N, dtype=torch.bfloat16, pin_memory=True)
     host_g.copy_(g)
     host_norm = torch.empty(1, dtype=torch.float32, pin_memory=True)
@@ -714,6 +715,9 @@ def measure_e2e(mp, st, g, opt, N, stream, device, kw, iters, step_no):
 
     ms = timed(pipelined, iters)
     del pipe
+    pipe = mp.HostGradPipeline(opt, device=device, transfer="engine")
+    ms_engine = timed(pipelined, max(3, iters // 2))
+    del pipe
     dev_g = torch.empty_like(g)
 
     def single_call():
@@ -726,8 +730,12 @@ def measure_e2e(mp, st, g, opt, N, stream, device, kw, iters, step_no):
     ms_single = timed(single_call, max(3, iters // 2))
     return {"value": round(N * iters / (ms / 1e3) / 1e9, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * N,
             "d2h_bytes_per_step": 8, "steps": iters, "ms_per_step": round(ms / iters, 5),
-            "h2d": "bf16 grads from pinned host memory by a copy engine, overlapped with the previous step's update",
-            "api": "HostGradPipeline.step -> Optimizer.step -> mp_optimizer_step (one C call per step)",
+            "h2d": "bf16 grads from pinned host memory copied by the SMs (mp_copy_from_host, one block per SM) "
+                   "beside the previous step's update",
+            "api": "HostGradPipeline.step -> mp_copy_from_host + Optimizer.step (mp_optimizer_step)",
+            "engine_copy": {"value": round(N * max(3, iters // 2) / (ms_engine / 1e3) / 1e9, 3),
+                            "ms_per_step": round(ms_engine / max(3, iters // 2), 5),
+                            "h2d": "the same pipeline with a copy engine (cudaMemcpyAsync) moving the gradients"},
             "single_call": {"value": round(N * max(3, iters // 2) / (ms_single / 1e3) / 1e9, 3),
                             "ms_per_step": round(ms_single / max(3, iters // 2), 5),
                             "h2d": "the norm kernel reads the pinned host gradients over the host link and "

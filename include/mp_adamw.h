@@ -431,6 +431,27 @@ int mp_optimizer_step(uint16_t* params, uint16_t* grads, const uint16_t* host_gr
                       float* host_norm, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Host-to-device copy by the SMs — for gradients that arrive in page-locked
+ * host memory. [LLMC] §3.3 hides transfers behind compute on a second
+ * stream; here the transfer of the next step's gradients runs beside the
+ * current step's update. The copy is a kernel of blocks_per_sm blocks of 256
+ * threads per SM issuing 16-B loads of the host buffer over the host link;
+ * with blocks_per_sm = 1 it fits beside the update kernel's resident blocks,
+ * so the two run concurrently when launched on different streams.
+ *
+ *   dst            device memory, `bytes` bytes, written.
+ *   host_src       page-locked host memory (cudaHostAlloc'd or
+ *                  cudaHostRegister'ed) the device can read; read only; must
+ *                  not change until the copy has run.
+ *   bytes          any count; 0 is a no-op. Both pointers 16-B aligned take
+ *                  the vector path; otherwise bytes are copied one by one.
+ *   blocks_per_sm  1 .. 32.
+ * Errors: MP_ERR_NULL, MP_ERR_RANGE, MP_ERR_ACCESS (host_src not page-locked
+ *         or not device-visible), MP_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int mp_copy_from_host(void* dst, const void* host_src, uint64_t bytes, int32_t blocks_per_sm, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Replayable steps: the step count on the device.
  *
  * mp_optimizer_step bakes t, seed and lr into its launches, so a recorded

@@ -93,6 +93,8 @@ def _load():
     L.mp_clip_scale_from_sumsq.argtypes = [vp, i32, f32, vp, vp, vp, vp]
     L.mp_lr_at.restype = ctypes.c_int
     L.mp_lr_at.argtypes = [ctypes.POINTER(MpLrSchedule), ctypes.c_int64, ctypes.POINTER(ctypes.c_float)]
+    L.mp_copy_from_host.restype = ctypes.c_int
+    L.mp_copy_from_host.argtypes = [vp, vp, u64, i32, vp]
     L.mp_adamw_step.restype = ctypes.c_int
     L.mp_adamw_step.argtypes = [vp, vp, vp, vp, vp, u64, u64, ctypes.POINTER(MpTensor), i32,
                                 f32, f32, f32, f32, f32, vp, i32, u32, vp, vp]
@@ -270,6 +272,24 @@ class LRSchedule:
         out = ctypes.c_float()
         _check(_lib.mp_lr_at(ctypes.byref(self._s), int(t), ctypes.byref(out)), "mp_lr_at")
         return out.value
+
+
+def mp_copy_from_host(dst: torch.Tensor, host_src: torch.Tensor, nbytes: Optional[int] = None,
+                      blocks_per_sm: int = 1, stream=None) -> None:
+    """Enqueue a host-to-device copy of page-locked host memory done by the
+    SMs (blocks_per_sm blocks of 256 threads per SM)."""
+    if not isinstance(dst, torch.Tensor) or not dst.is_cuda or not dst.is_contiguous():
+        raise ValueError("dst: contiguous CUDA tensor expected")
+    if not isinstance(host_src, torch.Tensor) or host_src.is_cuda or not host_src.is_contiguous():
+        raise ValueError("host_src: contiguous host tensor expected")
+    if dst.device.index != torch.cuda.current_device():
+        raise ValueError(f"dst: on {dst.device}, but the current device is cuda:{torch.cuda.current_device()}")
+    avail = min(dst.numel() * dst.element_size(), host_src.numel() * host_src.element_size())
+    nbytes = host_src.numel() * host_src.element_size() if nbytes is None else nbytes
+    if nbytes > avail:
+        raise ValueError(f"nbytes {nbytes} > {avail} bytes available")
+    _check(_lib.mp_copy_from_host(dst.data_ptr(), host_src.data_ptr(), nbytes, blocks_per_sm, _stream(stream)),
+           "mp_copy_from_host")
 
 
 def mp_grad_norm_noalloc(grads: torch.Tensor, clip: float, d_norm: torch.Tensor, d_scale: torch.Tensor,
@@ -585,19 +605,24 @@ class HostGradPipeline:
     with each step's host-to-device copy overlapped with the previous step's
     update.
 
-    Two device gradient buffers alternate: step t's copy (a copy engine, on
-    its own stream) fills buffer t % 2 while the compute stream still runs
-    step t - 1 on the other one; the step waits for its copy (an event), and
-    a copy waits for the step that last read its buffer. Every step is one
+    Two device gradient buffers alternate: step t's copy (on its own stream)
+    fills buffer t % 2 while the compute stream still runs step t - 1 on the
+    other one; the step waits for its copy (an event), and a copy waits for
+    the step that last read its buffer. transfer="kernel" (the default) copies
+    with mp_copy_from_host (one block per SM, beside the update kernel);
+    transfer="engine" with a copy engine (cudaMemcpyAsync). Every step is one
     Optimizer.step call (mp_optimizer_step) on the compute stream; the norm
     can be copied back to a page-locked host float each step. Nothing here
     synchronises the host, so a host buffer passed to step() must not be
     rewritten before its copy has run: wait on last_copy() (an event) first.
     """
 
-    def __init__(self, opt: "Optimizer", device=None):
+    def __init__(self, opt: "Optimizer", device=None, transfer: str = "kernel"):
+        if transfer not in ("kernel", "engine"):
+            raise ValueError("transfer: 'kernel' or 'engine'")
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.opt = opt
+        self.transfer = transfer
         self.buffers = [torch.empty(opt.n, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(dev)
         self.copied = [torch.cuda.Event() for _ in range(2)]
@@ -615,7 +640,10 @@ class HostGradPipeline:
         with torch.cuda.stream(self.copy_stream):
             if self.used[b] is not None:
                 self.copy_stream.wait_event(self.used[b])
-            buf.copy_(host_grads.view(buf.dtype), non_blocking=True)
+            if self.transfer == "kernel":
+                mp_copy_from_host(buf, host_grads, stream=self.copy_stream)
+            else:
+                buf.copy_(host_grads.view(buf.dtype), non_blocking=True)
             self.copied[b].record(self.copy_stream)
         compute.wait_event(self.copied[b])
         self.opt.step(params, buf, master, m, v, t, seed, stream=compute)
@@ -639,5 +667,5 @@ __all__ = [
     "mp_adamw_step", "mp_optimizer_step", "mp_outlier_state_bytes", "mp_outlier_reset", "mp_outlier_check",
     "mp_stochastic_round", "mp_stochastic_round_fp16", "mp_accumulate_sr", "mp_noise_u32", "mp_bias_table_len", "mp_bias_table", "mp_optimizer_step_graph",
     "MpStepState", "MpLaunch", "mp_step_launches", "LIB_PATH", "mp_grad_sumsq", "mp_clip_scale_from_sumsq",
-    "LRSchedule", "MpLrSchedule", "LR_KINDS", "HostGradPipeline",
+    "LRSchedule", "MpLrSchedule", "LR_KINDS", "HostGradPipeline", "mp_copy_from_host",
 ]

@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libmpadamw.so")
 # compute-free stream probes, a separate library that only the benchmark loads
 PROBE_LIB = os.path.join(PKG, "libmpprobe.so")
 
-SOURCES = ["mp_api.cu", "mp_step.cu", "mp_norm.cu", "mp_sr.cu", "mp_outlier.cu", "mp_small.cu"]
+SOURCES = ["mp_api.cu", "mp_step.cu", "mp_norm.cu", "mp_sr.cu", "mp_outlier.cu", "mp_small.cu", "mp_copy.cu"]
 PROBE_SOURCES = ["mp_probe.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [

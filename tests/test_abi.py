@@ -332,3 +332,12 @@ def test_lr_schedule_checks(mp):
         mp.LRSchedule("step", lr_max=1e-3)
     with pytest.raises(mp.MpError):
         mp.LRSchedule("cosine", lr_max=1e-3, warmup=5, total=5)
+
+
+def test_copy_from_host_argument_checks(mp):
+    L = mp.lib()
+    assert L.mp_copy_from_host(None, None, 0, 1, None) == mp.MP_OK  # nothing to copy
+    assert L.mp_copy_from_host(None, FAKE, 16, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_copy_from_host(FAKE, None, 16, 1, None) == mp.MP_ERR_NULL
+    assert L.mp_copy_from_host(FAKE, FAKE, 16, 0, None) == mp.MP_ERR_RANGE
+    assert L.mp_copy_from_host(FAKE, FAKE, 16, 33, None) == mp.MP_ERR_RANGE

@@ -154,7 +154,32 @@ def test_host_gradients_extreme_values_take_the_fp64_path(scale):
         assert _same(a[k], b[k]), k
 
 
-def test_host_gradient_pipeline_equals_device_gradient_steps():
+@pytest.mark.parametrize("nbytes,src_off,dst_off", [(0, 0, 0), (1, 0, 0), (15, 0, 0), (16, 0, 0),
+                                                     ((1 << 24) + 9, 0, 0), ((1 << 20) + 3, 3, 0),
+                                                     ((1 << 20) + 5, 0, 5), (1 << 22, 16, 32)])
+def test_copy_from_host_is_exact(nbytes, src_off, dst_off):
+    """mp_copy_from_host: every byte arrives, aligned (vectors plus a tail) or
+    not (byte by byte), and nothing outside the destination range changes."""
+    g = torch.Generator().manual_seed(nbytes)
+    host = torch.empty(nbytes + src_off, dtype=torch.uint8, pin_memory=True)
+    host.copy_(torch.randint(0, 256, (nbytes + src_off,), generator=g, dtype=torch.uint8))
+    dev = torch.full((nbytes + dst_off + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    mp.mp_copy_from_host(dev[dst_off:dst_off + max(nbytes, 1)], host[src_off:src_off + max(nbytes, 1)], nbytes)
+    torch.cuda.synchronize()
+    got = dev.cpu()
+    assert torch.equal(got[dst_off:dst_off + nbytes], host[src_off:src_off + nbytes])
+    assert bool((got[:dst_off] == 0xA5).all()) and bool((got[dst_off + nbytes:] == 0xA5).all())
+
+
+def test_copy_from_host_refuses_pageable_memory():
+    dev = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mp.MpError) as e:
+        mp.mp_copy_from_host(dev, torch.zeros(64, dtype=torch.uint8))  # not page-locked
+    assert e.value.status == mp.MP_ERR_ACCESS
+
+
+@pytest.mark.parametrize("transfer", ["kernel", "engine"])
+def test_host_gradient_pipeline_equals_device_gradient_steps(transfer):
     """HostGradPipeline: each step's gradients copied from page-locked host
     memory on a copy stream, overlapped with the previous step's update; 6
     steps with different gradients must equal the same steps on device
@@ -173,7 +198,7 @@ def test_host_gradient_pipeline_equals_device_gradient_steps():
         h.copy_(g)
     norms = [torch.empty(1, dtype=torch.float32, pin_memory=True) for _ in range(6)]
     opt_a = mp.Optimizer(tab, clip=H["clip"], **kw)
-    pipe = mp.HostGradPipeline(opt_a)
+    pipe = mp.HostGradPipeline(opt_a, transfer=transfer)
     for t in range(1, 7):
         pipe.step(a["params"], host[t - 1], a["master"], a["m"], a["v"], t, W.step_seed(t), host_norm=norms[t - 1])
     opt_b = mp.Optimizer(tab, clip=H["clip"], **kw)
@@ -191,7 +216,7 @@ def test_host_gradient_pipeline_equals_device_gradient_steps():
     d = {k: x.clone() for k, x in a.items()}
     opt_c = mp.Optimizer(tab, clip=H["clip"], **kw)
     opt_d = mp.Optimizer(tab, clip=H["clip"], **kw)
-    pipe_c = mp.HostGradPipeline(opt_c)
+    pipe_c = mp.HostGradPipeline(opt_c, transfer=transfer)
     one = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
     for t in range(7, 10):
         pipe_c.last_copy().synchronize()
