@@ -4,13 +4,13 @@
 // llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §3.3 hides
 // transfers behind compute on a second stream. Here the transfer is the next
 // step's gradients crossing the host link while the current step's update
-// streams through HBM. A copy engine does this at the link's rate on some
-// hosts and at half of it on others (measured: 91-211 GB/s for the same 16 GB
-// copy), while loads issued by the SMs keep many more requests in flight and
-// reach the link's rate more steadily. One block of 256 threads per SM at
-// 24-32 registers fits beside the update kernel's three resident blocks of 72
-// registers, so the copy runs concurrently with the update rather than after
-// it.
+// streams through HBM. Alone, a copy engine and SM loads both move pinned
+// host memory at the link's ~210 GB/s on GB300; but in some runs of pipelined
+// steps on the shared hosts, the copy engine's 16 GB took ~175 ms where SM
+// loads of the same buffer in the same process took ~92 ms. One block of 256
+// threads per SM, at a few dozen registers, fits beside the update kernel's
+// three resident blocks of 72 registers, so the copy runs concurrently with
+// the update rather than after it.
 #include <cstdint>
 
 #include "mp_adamw.h"
