@@ -6,7 +6,7 @@
 // step's gradients crossing the host link while the current step's update
 // streams through HBM. Alone, a copy engine and SM loads both move pinned
 // host memory at the link's ~210 GB/s on GB300; but in some runs of pipelined
-// steps on the shared hosts, the copy engine's 16 GB took ~175 ms where SM
+// steps on some GB300 hosts, the copy engine's 16 GB took ~175 ms where SM
 // loads of the same buffer in the same process took ~92 ms. One block of 256
 // threads per SM, at a few dozen registers, fits beside the update kernel's
 // three resident blocks of 72 registers, so the copy runs concurrently with
