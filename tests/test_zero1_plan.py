@@ -164,7 +164,7 @@ def _pow2_grads(rank, step, n):
     return (s * torch.exp2(k)).to(torch.bfloat16)
 
 
-def _dp_worker(rank, world, port, q):
+def _dp_worker(rank, world, port, q, with_master=True):
     """Three steps of ZeRO-1 (the driver, oracle arithmetic) and of plain data
     parallelism (all-reduce average, every rank the whole buffer) from the
     same state: the weights must agree bit for bit (CMU 11-667 lecture 13
@@ -178,33 +178,36 @@ def _dp_worker(rank, world, port, q):
         gen = torch.Generator().manual_seed(5)
         master0 = torch.randn(N, generator=gen) * 0.02
         zopt = Zero1Optimizer(TABLE, clip=1.0, device="cpu", kernels=OracleKernels(), **H)
-        z = zopt.make_shard_state(master0)
+        z = zopt.make_shard_state(master0, with_master=with_master)
         z_params = master0.to(torch.bfloat16)
-        d_params, d_master = master0.to(torch.bfloat16), master0.clone()
+        d_params, d_master = master0.to(torch.bfloat16), (master0.clone() if with_master else None)
         d_m, d_v = torch.zeros(N), torch.zeros(N)
         u16 = OracleKernels._u16
         for t in (1, 2, 3):
             g = _pow2_grads(rank, t, N)
-            zopt.step(z_params, g.clone(), z["master"], z["m"], z["v"], t=t, seed=100 + t)
+            zopt.step(z_params, g.clone(), z.get("master"), z["m"], z["v"], t=t, seed=100 + t)
             avg = g.clone()
             dist.all_reduce(avg, op=dist.ReduceOp.AVG)
             _, _, sc = oracle.grad_norm(u16(avg), 1.0)
-            assert oracle.adamw_step(u16(d_params), u16(avg), d_master.numpy(), d_m.numpy(), d_v.numpy(), 0, TABLE,
+            assert oracle.adamw_step(u16(d_params), u16(avg), d_master.numpy() if with_master else None,
+                                     d_m.numpy(), d_v.numpy(), 0, TABLE,
                                      H["lr"], H["beta1"], H["beta2"], H["eps"], H["weight_decay"], float(sc), t,
                                      100 + t) == 0
         sl = zopt.layout.slice()
         q.put((rank, torch.equal(z_params.view(torch.int16), d_params.view(torch.int16)),
-               torch.equal(z["master"], d_master[sl]), torch.equal(z["m"], d_m[sl]), torch.equal(z["v"], d_v[sl])))
+               torch.equal(z["master"], d_master[sl]) if with_master else True,
+               torch.equal(z["m"], d_m[sl]), torch.equal(z["v"], d_v[sl])))
     finally:
         dist.destroy_process_group()
 
 
-def test_zero1_equals_data_parallel_bit_for_bit_gloo():
+@pytest.mark.parametrize("with_master", [True, False])
+def test_zero1_equals_data_parallel_bit_for_bit_gloo(with_master):
     world = 2
     port = _free_port()
     ctx = mproc.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, q, with_master)) for r in range(world)]
     for p in procs:
         p.start()
     out = sorted(q.get(timeout=300) for _ in range(world))
