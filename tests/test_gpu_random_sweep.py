@@ -1,9 +1,11 @@
 """A seeded random sweep of the CUDA paths against the oracle, bit for bit:
 the update over a range (random sizes, global offsets up to 5·2^32, tables
-of 1 to 2^20-element tensors, unaligned buffers, both variants, betas,
-eps, lr, decay and step counts), the whole-step call (cluster kernel below
-32,768 params, the general path above), the standalone rounding to bf16
-and to fp16 and the accumulate-and-round, on values from 1e-40 to 1e38."""
+of 1 to 2^20-element tensors, unaligned buffers and vector-aligned buffers
+that start mid-line, both variants, betas, eps, lr, decay and step counts),
+the whole-step call (cluster kernel below 32,768 params, the general path
+above), the standalone rounding to bf16 and to fp16, the
+accumulate-and-round, on values from 1e-40 to 1e38; the ZeRO-1 norm over
+random shard counts; and host-to-device copies by the SMs."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,7 @@ if torch.cuda.is_available():
     __graft_entry__.build()
     import mixed_precision_adamw_gb300 as mp
 
-CASES = 200
+CASES = 280
 
 
 @pytest.fixture(autouse=True)
@@ -58,7 +60,7 @@ def _bits(t):
 def _update_case(rng, whole):
     n = int(rng.choice([1, 3, 8, 2047, 2048, 2049, 4100, 30000, 32768, 32769, 70001, 300007]))
     goff = 0 if whole else int(rng.choice([0, 4, 17, (1 << 32) - int(rng.integers(1, 3000)), 5 << 32]))
-    pad = int(rng.choice([0, 0, 0, 1, 2]))
+    pad = int(rng.choice([0, 0, 0, 1, 2, 4, 12, 28]))  # 4, 12, 28: vector path, tiles after a peeled head
     seed = int(rng.integers(0, 1 << 32))
     gen = torch.Generator().manual_seed(int(rng.integers(0, 1 << 30)))
     tmax = int(rng.choice([1, 7, 100, 5000, 1 << 20]))
@@ -97,14 +99,57 @@ def _update_case(rng, whole):
         assert np.array_equal(_bits(d[k]), host[k].view(np.uint32)), (k, what)
 
 
+def _zero1_norm_case(rng):
+    """Per-shard sums of squares (mp_grad_sumsq) combined in rank order
+    (mp_clip_scale_from_sumsq): the same bits as the oracle's ZeRO-1 norm of
+    those sums, and each sum within 1e-6 of the oracle's own."""
+    world = int(rng.choice([1, 2, 3, 8, 16]))
+    per = int(rng.choice([1, 5, 2048, 4099, 100_003]))
+    pad = int(rng.choice([0, 1, 4]))
+    g = _bf16(rng.standard_normal(world * per) * 10.0 ** rng.uniform(-5, 1))
+    dg = _dev16(g, pad)
+    ws = torch.empty(max(8, mp.mp_grad_norm_workspace_bytes(per)), dtype=torch.uint8, device="cuda")
+    parts = torch.empty(world, dtype=torch.float64, device="cuda")
+    for r in range(world):
+        mp.mp_grad_sumsq(dg[r * per:(r + 1) * per], ws, parts[r:r + 1])
+    clip = float(rng.choice([0.5, 1.0, 100.0]))
+    d_norm, d_scale = torch.empty(1, device="cuda"), torch.empty(1, device="cuda")
+    total = torch.empty(1, dtype=torch.float64, device="cuda")
+    mp.mp_clip_scale_from_sumsq(parts, clip, d_norm, d_scale, total)
+    torch.cuda.synchronize()
+    gp = parts.cpu().numpy()
+    s, nrm, sc = oracle.norm_from_parts(gp, clip)
+    assert total.item() == s and np.float32(d_norm.item()) == nrm and np.float32(d_scale.item()) == sc, (world, per)
+    for r in range(world):
+        ref = oracle.sumsq(g[r * per:(r + 1) * per])
+        assert abs(gp[r] - ref) <= 1e-6 * ref, (world, per, r)
+
+
+def _copy_case(rng):
+    nbytes = int(rng.choice([1, 15, 16, 17, 4096, 100_003, 1 << 22]))
+    so, do = int(rng.choice([0, 1, 8, 16])), int(rng.choice([0, 3, 16]))
+    host = torch.empty(nbytes + so, dtype=torch.uint8, pin_memory=True)
+    host.copy_(torch.from_numpy(rng.integers(0, 256, nbytes + so, dtype=np.uint8)))
+    dev = torch.zeros(nbytes + do, dtype=torch.uint8, device="cuda")
+    mp.mp_copy_from_host(dev[do:], host[so:], nbytes, blocks_per_sm=int(rng.choice([1, 2, 4])))
+    torch.cuda.synchronize()
+    assert torch.equal(dev[do:].cpu(), host[so:]), (nbytes, so, do)
+
+
 def test_random_sweep_against_the_oracle():
     rng = np.random.default_rng(20261202)
-    counts = dict(step=0, whole=0, sr=0, acc=0, sr16=0)
+    counts = dict(step=0, whole=0, sr=0, acc=0, sr16=0, zero1=0, copy=0)
     for _ in range(CASES):
-        kind = str(rng.choice(["step", "whole", "sr", "acc", "sr16"]))
+        kind = str(rng.choice(list(counts)))
         counts[kind] += 1
         if kind in ("step", "whole"):
             _update_case(rng, kind == "whole")
+            continue
+        if kind == "zero1":
+            _zero1_norm_case(rng)
+            continue
+        if kind == "copy":
+            _copy_case(rng)
             continue
         n = int(rng.choice([1, 7, 2049, 30001, 300007]))
         goff = int(rng.choice([0, 17, (1 << 32) - int(rng.integers(1, 3000))]))
@@ -126,4 +171,4 @@ def test_random_sweep_against_the_oracle():
             ref = acc0.copy()
             oracle.accumulate_sr(ref, x, goff, seed)
             assert np.array_equal(_u16(acc), ref), (n, goff, pad)
-    assert min(counts.values()) >= 20, counts
+    assert min(counts.values()) >= 15, counts
