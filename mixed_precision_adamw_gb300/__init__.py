@@ -615,7 +615,12 @@ class HostGradPipeline:
     can be copied back to a page-locked host float each step. Nothing here
     synchronises the host, so a host buffer passed to step() must not be
     rewritten before its copy has run: wait on last_copy() (an event) first.
+    Below SMALL_N parameters a copy takes less time than this bookkeeping, so
+    each step is instead one Optimizer.step call whose norm kernel reads the
+    host gradients itself (the same results).
     """
+
+    SMALL_N = 1 << 20
 
     def __init__(self, opt: "Optimizer", device=None, transfer: str = "kernel"):
         if transfer not in ("kernel", "engine"):
@@ -626,8 +631,9 @@ class HostGradPipeline:
         self.buffers = [torch.empty(opt.n, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(dev)
         self.copied = [torch.cuda.Event() for _ in range(2)]
-        self.used = [None, None]  # event after the last step that read each buffer
+        self.used = [torch.cuda.Event() for _ in range(2)]  # after the last step that read each buffer
         self.k = 0
+        self.small = opt.n <= self.SMALL_N
 
     def step(self, params, host_grads: torch.Tensor, master, m, v, t: int, seed: int, host_norm=None,
              stream=None):
@@ -637,8 +643,13 @@ class HostGradPipeline:
         b = self.k % 2
         self.k += 1
         buf = self.buffers[b]
+        if self.small:
+            self.opt.step(params, buf, master, m, v, t, seed, host_grads=host_grads, host_norm=host_norm,
+                          stream=compute)
+            self.copied[b].record(compute)
+            return
         with torch.cuda.stream(self.copy_stream):
-            if self.used[b] is not None:
+            if self.k > 2:  # the buffer's previous reader, two steps back
                 self.copy_stream.wait_event(self.used[b])
             if self.transfer == "kernel":
                 mp_copy_from_host(buf, host_grads, stream=self.copy_stream)
@@ -650,9 +661,7 @@ class HostGradPipeline:
         if host_norm is not None:
             with torch.cuda.stream(compute):
                 host_norm.copy_(self.opt.d_norm, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(compute)
-        self.used[b] = ev
+        self.used[b].record(compute)
 
     def last_copy(self) -> torch.cuda.Event:
         """The event recorded after the latest step's host-to-device copy: once

@@ -178,13 +178,14 @@ def test_copy_from_host_refuses_pageable_memory():
     assert e.value.status == mp.MP_ERR_ACCESS
 
 
-@pytest.mark.parametrize("transfer", ["kernel", "engine"])
-def test_host_gradient_pipeline_equals_device_gradient_steps(transfer):
+@pytest.mark.parametrize("transfer,n_params", [("kernel", (1 << 22) + 12345), ("engine", (1 << 22) + 12345),
+                                               ("kernel", 100_003)])
+def test_host_gradient_pipeline_equals_device_gradient_steps(transfer, n_params):
     """HostGradPipeline: each step's gradients copied from page-locked host
     memory on a copy stream, overlapped with the previous step's update; 6
     steps with different gradients must equal the same steps on device
     gradients bit for bit, and the host norms must be each step's norm."""
-    tab, st, _ = _setup()
+    tab, st, _ = _setup(n_params)
     H = W.HYPER
     kw = dict(lr=H["lr"], beta1=H["beta1"], beta2=H["beta2"], eps=H["eps"], weight_decay=H["weight_decay"])
     n = st["m"].numel()
