@@ -286,3 +286,36 @@ def test_zero1_one_nccl_rank_equals_single_gpu_step():
                 assert torch.equal(zst[k].view(torch.int32), ref[k].view(torch.int32)), k
     finally:
         dist.destroy_process_group()
+
+
+def test_degenerate_norm_halves_and_empty_update():
+    """Empty and degenerate inputs of the ZeRO-1 norm's halves and the update:
+    an empty shard sums to 0; all-zero sums give norm 0 and scale 1; a
+    non-finite sum gives a NaN scale; an empty update writes nothing. The
+    oracle's ZeRO-1 norm agrees on each."""
+    ws = torch.empty(64, dtype=torch.uint8, device=DEV)
+    g = torch.zeros(16, dtype=torch.bfloat16, device=DEV)
+    parts = torch.full((3,), -1.0, dtype=torch.float64, device=DEV)
+    mp.mp_grad_sumsq(g, ws, parts[0:1], n=0)
+    parts[1:] = 0.0
+    d_norm, d_scale = torch.full((1,), -1.0, device=DEV), torch.full((1,), -1.0, device=DEV)
+    mp.mp_clip_scale_from_sumsq(parts, 1.0, d_norm, d_scale)
+    torch.cuda.synchronize()
+    assert parts[0].item() == 0.0
+    _, nrm, sc = oracle.norm_from_parts([0.0, 0.0, 0.0], 1.0)
+    assert (np.float32(d_norm.item()), np.float32(d_scale.item())) == (nrm, sc) == (0.0, 1.0)
+    for bad in (float("inf"), float("nan")):
+        parts[2] = bad
+        mp.mp_clip_scale_from_sumsq(parts, 1.0, d_norm, d_scale)
+        torch.cuda.synchronize()
+        assert np.isnan(d_scale.item()) and np.isnan(oracle.norm_from_parts(parts.cpu().numpy(), 1.0)[2])
+    # an empty update over a non-empty table: nothing written, no device error
+    st = {k: torch.full((8,), 3.0, dtype=torch.float32, device=DEV) for k in ("master", "m", "v")}
+    params = torch.full((8,), 3.0, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mp.mp_adamw_step(params, params.clone(), st["master"], st["m"], st["v"], mp.TensorTable([(0, 8, 1)]), lr=1e-3,
+                     beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, d_grad_scale=None, t=1, seed=1,
+                     global_offset=3, n=0, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and bool((params.float() == 3.0).all())
+    assert all(bool((x == 3.0).all()) for x in st.values())
