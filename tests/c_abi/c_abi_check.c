@@ -5,12 +5,15 @@
  *
  * One optimizer step (mp_optimizer_step, then a second call of the pieces:
  * mp_grad_norm + mp_adamw_step) on n = 100,003 elements split into 7 tensors
- * with alternating decay flags, then mp_stochastic_round, mp_accumulate_sr and
+ * with alternating decay flags, against the oracle's own norm, clip scale
+ * and steps; then mp_stochastic_round, mp_accumulate_sr and
  * mp_stochastic_round_fp16.
  * Then steps 3-6 as replayable steps: step 3 a plain mp_optimizer_step_graph
  * call, steps 4-6 replays of one CUDA graph captured from a stream, with
- * fresh gradients copied in between. Exit status 0 when every output is
- * bit-identical to the oracle's.
+ * fresh gradients copied in between. Then the ZeRO-1 norm's two halves over
+ * 4 shards, the learning-rate schedules and a host-to-device copy by the SMs.
+ * Exit status 0 when every output is bit-identical to the oracle's (and the
+ * copy to its source).
  */
 #include <math.h>
 #include <stdint.h>
@@ -126,18 +129,22 @@ int main(void) {
     CK(cudaMemcpy(out_sr, d_sr, sizeof out_sr, cudaMemcpyDeviceToHost));
     CK(cudaMemcpy(out_h, d_h, sizeof out_h, cudaMemcpyDeviceToHost));
 
-    /* the oracle, with the GPU's clip scales (the norms are checked to 1e-6) */
+    /* the oracle's own chain: its norm and clip scale, then its steps. The GPU's
+     * norm must be within 1e-6 of the oracle's fp64 one; the fp32 norms (and so
+     * the scales) then agree except within ~1e-9 of a rounding boundary, and
+     * the step is required to match bit for bit. */
     double sumsq;
     float norm_o, scale_o;
     oracle_grad_norm(grads, N, hyper.clip, &sumsq, &norm_o, &scale_o);
-    if (!(fabs((double)norm1 - sqrt(sumsq)) <= 1e-6 * sqrt(sumsq)) || scale1 != oracle_clip_scale(norm1, 1.0f)) {
-        fprintf(stderr, "norm %.9g vs oracle %.9g\n", norm1, sqrt(sumsq));
+    if (!(fabs((double)norm1 - sqrt(sumsq)) <= 1e-6 * sqrt(sumsq)) || scale1 != scale_o || scale2 != scale_o) {
+        fprintf(stderr, "norm %.9g scale %.9g/%.9g vs oracle %.9g %.9g\n", norm1, scale1, scale2, sqrt(sumsq),
+                scale_o);
         return 1;
     }
     if (oracle_adamw_step(params_o, grads, master_o, m_o, v_o, 0, N, otable, NT, hyper.lr, hyper.beta1,
-                          hyper.beta2, hyper.eps, hyper.weight_decay, scale1, 1, 11) != 0 ||
+                          hyper.beta2, hyper.eps, hyper.weight_decay, scale_o, 1, 11) != 0 ||
         oracle_adamw_step(params_o, grads, master_o, m_o, v_o, 0, N, otable, NT, hyper.lr, hyper.beta1,
-                          hyper.beta2, hyper.eps, hyper.weight_decay, scale2, 2, 12) != 0)
+                          hyper.beta2, hyper.eps, hyper.weight_decay, scale_o, 2, 12) != 0)
         return 1;
     oracle_stochastic_round(out_sr_o, master_o, 0, N, 99);
     oracle_accumulate_sr(out_sr_o, master_o, 0, N, 98);
@@ -219,6 +226,65 @@ int main(void) {
     ok &= same(master, master_o, sizeof master, "master after graph steps");
     ok &= same(m, m_o, sizeof m, "m after graph steps");
     ok &= same(v, v_o, sizeof v, "v after graph steps");
+
+    /* the ZeRO-1 norm in two halves: 4 shards' sums of squares, then the
+     * scale from them in rank order; the oracle's ZeRO-1 norm of the same
+     * sums must match bit for bit, and each sum the oracle's own to 1e-6 */
+    enum { W = 4 };
+    const uint32_t per = N / W; /* the last N % W elements are left out */
+    double *d_parts, *d_total;
+    double gpu_parts[W], total;
+    CK(cudaMalloc((void**)&d_parts, sizeof gpu_parts));
+    CK(cudaMalloc((void**)&d_total, sizeof total));
+    CK(cudaMemcpy(d_grads, grads_k[0], sizeof grads, cudaMemcpyHostToDevice));
+    for (int r = 0; r < W; ++r) MP(mp_grad_sumsq(d_grads + (size_t)r * per, per, d_ws, ws_bytes, d_parts + r, NULL));
+    MP(mp_clip_scale_from_sumsq(d_parts, W, 0.25f, d_norm, d_scale, d_total, NULL));
+    float zn, zs;
+    CK(cudaMemcpy(gpu_parts, d_parts, sizeof gpu_parts, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&total, d_total, sizeof total, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&zn, d_norm, 4, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(&zs, d_scale, 4, cudaMemcpyDeviceToHost));
+    double zsum_o;
+    float zn_o, zs_o;
+    oracle_norm_from_parts(gpu_parts, W, 0.25f, &zsum_o, &zn_o, &zs_o);
+    if (total != zsum_o || zn != zn_o || zs != zs_o) {
+        fprintf(stderr, "ZeRO-1 norm %.9g scale %.9g vs oracle %.9g %.9g\n", zn, zs, zn_o, zs_o);
+        ok = 0;
+    }
+    for (int r = 0; r < W; ++r) {
+        const double ref = oracle_sumsq(grads_k[0] + (size_t)r * per, per);
+        if (!(fabs(gpu_parts[r] - ref) <= 1e-6 * ref)) {
+            fprintf(stderr, "shard %d sum of squares %.17g vs oracle %.17g\n", r, gpu_parts[r], ref);
+            ok = 0;
+        }
+    }
+    cudaFree(d_parts);
+    cudaFree(d_total);
+
+    /* learning-rate schedules (host only): every step of four runs */
+    for (int kind = MP_LR_CONSTANT; kind <= MP_LR_WSD; ++kind) {
+        const mp_lr_schedule_t sch = {kind, 0, 50, 1000, 6e-4f, 6e-5f, 0.2f, 0.0f};
+        for (int64_t t = 1; t <= 1100; ++t) {
+            float lr;
+            MP(mp_lr_at(&sch, t, &lr));
+            const float lr_o = oracle_lr(kind, 50, 1000, 6e-4f, 6e-5f, 0.2f, t);
+            if (memcmp(&lr, &lr_o, 4) != 0) {
+                fprintf(stderr, "schedule %d step %lld: lr %.9g vs oracle %.9g\n", kind, (long long)t, lr, lr_o);
+                ok = 0;
+                break;
+            }
+        }
+    }
+
+    /* a host-to-device copy by the SMs from page-locked memory */
+    uint16_t* h_pinned;
+    CK(cudaHostAlloc((void**)&h_pinned, sizeof grads, cudaHostAllocDefault));
+    memcpy(h_pinned, grads_k[1], sizeof grads);
+    CK(cudaMemset(d_grads, 0, sizeof grads));
+    MP(mp_copy_from_host(d_grads, h_pinned, sizeof grads, 1, NULL));
+    CK(cudaMemcpy(grads, d_grads, sizeof grads, cudaMemcpyDeviceToHost));
+    ok &= same(grads, grads_k[1], sizeof grads, "host-to-device copy by the SMs");
+    cudaFreeHost(h_pinned);
     printf("c_abi_check: %s (n=%u, norm %.7g, scale %.7g; graph steps %d-%d)\n",
            ok ? "bit-identical to the oracle" : "MISMATCH", N, norm1, scale1, FIRST, LAST);
     cudaGraphExecDestroy(exec); cudaGraphDestroy(graph); cudaStreamDestroy(stream); free(bias);

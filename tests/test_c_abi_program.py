@@ -1,9 +1,10 @@
 """libmpadamw.so used from plain C: tests/c_abi/c_abi_check.c allocates its
 own device buffers, calls the ABI (mp_optimizer_step, mp_grad_norm,
-mp_adamw_step, mp_stochastic_round, and mp_optimizer_step_graph captured
-into a CUDA graph with the runtime's own stream capture) and compares every
-output bit for bit with the CPU oracle linked into the same program. No Python or PyTorch on
-that path. On CPU the program is only compiled and linked (the header is
+mp_adamw_step, the roundings, mp_optimizer_step_graph captured into a CUDA
+graph with the runtime's own stream capture, the ZeRO-1 norm's two halves,
+mp_lr_at and mp_copy_from_host) and compares every output bit for bit with
+the CPU oracle linked into the same program, which computes its own norm,
+clip scale and steps. No Python or PyTorch on that path. On CPU the program is only compiled and linked (the header is
 valid C and every symbol resolves); on a GPU it runs."""
 import os
 import shutil
