@@ -1,4 +1,5 @@
-"""Property-based pins of the oracle's stochastic rounding (CPU only).
+"""Property-based pins of the oracle's stochastic rounding, learning-rate
+schedules and ZeRO-1 norm (CPU only).
 
 For any fp32 value and any 16-bit draw, the rounding to bf16 and to fp16
 (llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §2.3: keep the
@@ -208,3 +209,59 @@ def test_one_step_tracks_torch_adamw_fp64(b1, b2, lr, eps, wd, t, scale, decay, 
 def W_bf16(x32: np.ndarray) -> np.ndarray:
     """bf16 patterns of fp32 values by torch's round-to-nearest cast."""
     return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# Learning-rate schedules and the ZeRO-1 norm (llm.c ch. 04 §4): properties
+# over drawn arguments.
+# --------------------------------------------------------------------------
+# lr_min = frac * lr_max with frac 0 or at least 1e-6: the schedules' double
+# arithmetic (lr_max - (lr_max - lr_min) * p) returns lr_min at the end only
+# while lr_min is not far below lr_max's rounding error.
+SCHED = st.tuples(st.integers(0, 3), st.integers(0, 400), st.integers(1, 20_000),
+                  st.floats(1e-6, 1.0), st.one_of(st.just(0.0), st.floats(1e-6, 1.0)), st.floats(0.01, 1.0))
+
+
+@settings(max_examples=300, deadline=None)
+@given(SCHED)
+def test_lr_schedule_stays_between_its_bounds_and_moves_one_way(args):
+    kind, warmup, span, hi, frac_lo, f = args
+    lo = float(np.float32(hi * frac_lo))
+    hi32 = float(np.float32(hi))
+    total = warmup + span
+    ulp = 2.0 ** -23
+    prev = None
+    ts = sorted(set([1, warmup, warmup + 1, total, total + 5] + list(range(1, total + 2, max(1, total // 60)))))
+    for t in [t for t in ts if t >= 1]:
+        x = float(oracle.lr(kind, warmup, total, hi, lo, f, t))
+        if t <= warmup:
+            assert 0.0 < x <= hi32 * (1 + ulp)
+            if prev is not None and prev[0] <= warmup:
+                assert x >= prev[1] * (1 - ulp)  # the warm-up rises
+        else:
+            assert lo * (1 - ulp) <= x <= hi32 * (1 + ulp)
+            if prev is not None and prev[0] > warmup:
+                assert x <= prev[1] * (1 + ulp)  # after it, nothing rises
+            if kind == 0:
+                assert x == hi32
+            if t >= total and kind != 0:
+                assert x == np.float32(lo)
+        prev = (t, x)
+
+
+@settings(max_examples=500, deadline=None)
+@given(st.lists(st.floats(0.0, 1e30), min_size=1, max_size=64), st.floats(1e-3, 1e3))
+def test_zero1_norm_is_the_rank_sum_within_rounding(parts, clip):
+    s, nrm, sc = oracle.norm_from_parts(parts, clip)
+    exact = math.fsum(parts)
+    assert abs(s - exact) <= len(parts) * 2.0 ** -53 * exact
+    # the norm is the float rounding of the sum's square root (below fp32's
+    # range that is a subnormal or zero: half its spacing, 2^-150, at most)
+    r = math.sqrt(s)
+    assert abs(float(nrm) - r) <= max(2.0 ** -24 * r, 2.0 ** -150)
+    # and the clip scale follows the rule min(1, clip / norm) in fp32
+    if float(nrm) == 0.0:
+        assert sc == 1.0
+    else:
+        q = np.float32(np.float32(clip) / nrm)
+        assert sc == min(np.float32(1.0), q)
