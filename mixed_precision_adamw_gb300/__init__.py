@@ -639,6 +639,8 @@ class HostGradPipeline:
              stream=None):
         if host_grads.is_cuda or not host_grads.is_pinned():
             raise ValueError("host_grads: page-locked host memory expected")
+        if host_grads.dtype not in _BF16_LIKE or host_grads.numel() != self.opt.n or not host_grads.is_contiguous():
+            raise ValueError(f"host_grads: {self.opt.n} contiguous bf16 values expected")
         compute = stream if stream is not None else torch.cuda.current_stream(self.buffers[0].device)
         b = self.k % 2
         self.k += 1

@@ -229,3 +229,8 @@ def test_host_gradient_pipeline_equals_device_gradient_steps(transfer, n_params)
         assert _same(c[k], d[k]), k
     with pytest.raises(ValueError):
         pipe.step(a["params"], grads[0], a["master"], a["m"], a["v"], 7, 7)  # device tensor, not pinned host
+    with pytest.raises(ValueError):  # one gradient short of the parameter set
+        pipe.step(a["params"], host[0][:-1], a["master"], a["m"], a["v"], 7, 7)
+    with pytest.raises(ValueError):  # fp32 values, not bf16 patterns
+        pipe.step(a["params"], torch.zeros(n, dtype=torch.float32, pin_memory=True), a["master"], a["m"], a["v"],
+                  7, 7)
