@@ -65,7 +65,12 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context only)
 STEP_KERNEL_SOURCES = ["mixed_precision_adamw_gb300/csrc/mp_step.cu",
                        "mixed_precision_adamw_gb300/csrc/mp_step.cuh",
-                       "mixed_precision_adamw_gb300/csrc/mp_device.cuh"]
+                       "mixed_precision_adamw_gb300/csrc/mp_device.cuh",
+                       "mixed_precision_adamw_gb300/csrc/mp_tma.cuh"]
+# The library runs a step launch through its TMA-staged kernel (one block per
+# SM, tiles of 2304 elements with master) when the launch holds at least two
+# tiles per SM; shorter launches take the register kernel. Used for labels only.
+TMA_TILE_MASTER = 2304
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "adamw_step_traffic.json")
 KERNEL_SAMPLES = 16  # event-bracketed step calls after the timed region, at least
 
@@ -115,6 +120,12 @@ def measured_hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_kernel_name(launch_elems: float, device) -> str:
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    tma = launch_elems >= 2 * sms * TMA_TILE_MASTER + 64
+    return "adamw_tma_kernel<master>" if tma else "adamw_vec_kernel<master>"
 
 
 def kernel_source_hash() -> str:
@@ -280,7 +291,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_hbm_peak()
     achieved = STEP_BYTES_MASTER * N / (step_kernel_ms / 1e3) / 1e9
     traffic, traffic_from = profiled_traffic_bytes(N / launches) if not args.params else (None, None)
-    roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master>", "achieved": round(achieved, 1),
+    roofline = {"bound": "hbm", "kernel": step_kernel_name(N / launches, device), "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": traffic,
                 "traffic_source": (f"ncu capture of a {traffic_from}-element launch (profiles/adamw_step_traffic.json), "
@@ -423,7 +434,7 @@ def run_zero1(args, world, rank, local):
     peak, peak_kind = measured_hbm_peak()
     achieved = STEP_BYTES_MASTER * per / ms / 1e6
     traffic, traffic_from = profiled_traffic_bytes(per / launches) if not args.params else (None, None)
-    roofline = {"bound": "hbm", "kernel": "adamw_vec_kernel<master> (this rank's shard)",
+    roofline = {"bound": "hbm", "kernel": step_kernel_name(per / launches, device) + " (this rank's shard)",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_kind": peak_kind, "traffic": traffic,
                 "algorithmic_bytes_per_launch": round(STEP_BYTES_MASTER * per / launches),
@@ -571,6 +582,9 @@ def measure_stream_probes(st, g, N, stream, peak):
     vp, u64, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int
     lib.mp_probe_step_streams.argtypes = [vp, vp, vp, vp, vp, u64, i32, vp]
     lib.mp_probe_copy.argtypes = [vp, vp, u64, i32, vp]
+    lib.mp_probe_step_streams_bulk.argtypes = [vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp]
+    lib.mp_probe_copy_bulk.argtypes = [vp, vp, u64, i32, i32, i32, vp, vp]
+    err = torch.zeros(1, dtype=torch.int32, device=g.device)
     chunk = 201_326_592  # the step's launch size on the large sets (whole 2048-element tiles)
     n = N // 2048 * 2048
     out = {}
@@ -586,6 +600,20 @@ def measure_stream_probes(st, g, N, stream, peak):
         out[f"step_streams_{bps}_blocks_per_sm"] = {"gbs": round(STEP_BYTES_MASTER * n / ms / 1e6, 1),
                                                     "frac": round(STEP_BYTES_MASTER * n / ms / 1e6 / peak, 4),
                                                     "ms": round(ms, 5)}
+    # the same streams staged through shared memory by TMA bulk copies
+    for bps, stages, hint in ((1, 4, 1), (1, 7, 1), (1, 7, 0), (2, 3, 1)):
+        def run_bulk():
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                rc = lib.mp_probe_step_streams_bulk(st["params"][a:].data_ptr(), g[a:].data_ptr(),
+                                                    st["master"][a:].data_ptr(), st["m"][a:].data_ptr(),
+                                                    st["v"][a:].data_ptr(), b - a, bps, stages, hint,
+                                                    err.data_ptr(), stream.cuda_stream)
+                assert rc == 0, rc
+        ms = time_events(run_bulk, 5, stream)
+        key = f"step_streams_tma_bulk_{bps}_blocks_per_sm_{stages}_stages" + ("_evict_first" if hint else "")
+        out[key] = {"gbs": round(STEP_BYTES_MASTER * n / ms / 1e6, 1),
+                    "frac": round(STEP_BYTES_MASTER * n / ms / 1e6 / peak, 4), "ms": round(ms, 5)}
     nbytes = min(STEP_BYTES_MASTER // 2 * N, 1 << 32) // 16 * 16
     src = torch.empty(nbytes, dtype=torch.uint8, device=g.device)
     dst = torch.empty_like(src)
@@ -595,9 +623,25 @@ def measure_stream_probes(st, g, N, stream, peak):
                                                    stream.cuda_stream), 10, stream)
         out[f"copy_16B_{bps}_blocks_per_sm"] = {"gbs": round(2 * nbytes / ms / 1e6, 1),
                                                 "frac": round(2 * nbytes / ms / 1e6 / peak, 4), "ms": round(ms, 5)}
+    tile_bytes = 2048 * 14
+    tiles = nbytes // tile_bytes
+    for bps, stages, hint in ((1, 7, 1), (2, 3, 1)):
+        def run_copy_bulk():
+            rc = lib.mp_probe_copy_bulk(dst.data_ptr(), src.data_ptr(), tiles, bps, stages, hint, err.data_ptr(),
+                                        stream.cuda_stream)
+            assert rc == 0, rc
+        ms = time_events(run_copy_bulk, 10, stream)
+        gbs = 2 * tiles * tile_bytes / ms / 1e6
+        out[f"copy_tma_bulk_{bps}_blocks_per_sm_{stages}_stages_evict_first"] = {
+            "gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "ms": round(ms, 5)}
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("a TMA bulk probe gave up waiting on its mbarrier")
     del src, dst
     out["what"] = ("compute-free SM kernels: the step's streams (28 B/param, written back unchanged) in "
-                   f"launches of {chunk} params, and a 16-B copy of {nbytes} bytes")
+                   f"launches of {chunk} params, through registers and through TMA bulk copies staged in "
+                   f"shared memory (one issuing thread per block, 28 KB stages); a 16-B copy of {nbytes} bytes "
+                   "and a TMA bulk copy of its whole 28 KB tiles")
     return out
 
 

@@ -72,11 +72,14 @@ extern "C" int mp_copy_from_host(void* dst, const void* host_src, uint64_t bytes
   const unsigned grid = static_cast<unsigned>(dev.sms * blocks_per_sm);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* d = static_cast<uint8_t*>(dst);
+  static std::atomic<bool> carve_vec[64], carve_bytes[64];
   if (reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(d) % 16 == 0) {
+    mpk::prefer_max_shared(mpk::copy_from_host_kernel, carve_vec);
     const uint64_t nvec = bytes / 16, done = nvec * 16;
     e = mpk::launch_pdl(mpk::copy_from_host_kernel, grid, mpk::kThreads, s, reinterpret_cast<uint4*>(d),
                         reinterpret_cast<const uint4*>(src), nvec, d + done, src + done, bytes - done);
   } else {
+    mpk::prefer_max_shared(mpk::copy_from_host_bytes_kernel, carve_bytes);
     e = mpk::launch_pdl(mpk::copy_from_host_bytes_kernel, grid, mpk::kThreads, s, d, src, bytes);
   }
   if (e != cudaSuccess) return mpk::record_cuda_error(e);

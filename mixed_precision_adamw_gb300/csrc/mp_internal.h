@@ -2,6 +2,7 @@
 // kernel launchers (mp_step.cu, mp_norm.cu, mp_sr.cu). Not installed.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <utility>
 
@@ -77,6 +78,45 @@ cudaError_t launch_pdl(void (*kernel)(Params...), unsigned grid, unsigned block,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch_pdl with `smem` bytes of dynamic shared memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_smem(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                            cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Asks the GPU to keep the largest shared-memory carve-out on SMs that run
+// `kernel`. The TMA-staged step kernel needs most of an SM's shared memory;
+// an SM whose carve-out was set small by another kernel's blocks must drain
+// before it can take one of its blocks, so a persistent kernel beside it (the
+// host-gradient copy) or just before it (the norm) would otherwise serialise
+// with it. Once per kernel (`done` belongs to that kernel) and device; a hint,
+// so a failure is ignored.
+template <typename... Params>
+void prefer_max_shared(void (*kernel)(Params...), std::atomic<bool> (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  if (dev < 0 || dev >= 64 || done[dev].load(std::memory_order_relaxed)) return;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    cudaGetLastError();
+  else
+    done[dev].store(true, std::memory_order_relaxed);
 }
 
 struct DeviceInfo {

@@ -93,6 +93,10 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
                         float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream,
                         uint16_t* copy_out, const StepClock* clock) {
   const StepClock c = clock != nullptr ? *clock : StepClock{nullptr, nullptr, 0, nullptr};
+  static std::atomic<bool> carve_plain[64], carve_copy[64], carve_finalize[64];
+  if (copy_out == nullptr) prefer_max_shared(norm_partial_kernel<false>, carve_plain);
+  else prefer_max_shared(norm_partial_kernel<true>, carve_copy);
+  prefer_max_shared(norm_finalize_kernel, carve_finalize);
   cudaError_t e = copy_out == nullptr
                       ? launch_pdl(norm_partial_kernel<false>, static_cast<unsigned>(nblocks), kThreads, stream,
                                    grads, n, vec ? 1 : 0, partials, copy_out)

@@ -270,4 +270,51 @@ __device__ __forceinline__ void vec_tiles(const StepArgs& p, const SegTable<CAP>
   for (uint64_t i = tail0; i < p.n; i += stride_tail) elem_update<kMaster>(p, segs, c, i, scale, h, seed);
 }
 
+// ---- tiles staged in shared memory (the TMA path, mp_step.cu) ---------------
+// One stage holds a whole 2048-element tile of every input stream, loaded by
+// the TMA engine; the update runs on it in place and the TMA engine stores
+// the results from it. Byte offsets within a stage:
+template <bool kMaster, uint32_t T>
+struct TmaStage {
+  static_assert(T % 64 == 0, "every stream's tile must span whole 128-B lines");
+  static constexpr uint32_t kTileElems = T;
+  static constexpr uint32_t kGrads = 0;   // bf16 gradients; with master, the rounded weights go here
+  static constexpr uint32_t kW = T * 2;   // the old weights: fp32 master, or the bf16 params in place
+  static constexpr uint32_t kM = kW + T * (kMaster ? 4 : 2);
+  static constexpr uint32_t kV = kM + T * 4;
+  static constexpr uint32_t kBytes = kV + T * 4;  // 14 B per element with master, 12 B without
+};
+
+// Updates group g (elements 4g .. 4g + 3) of the tile staged at `sp`, whose
+// element 0 is element e0 of the launch: reads the inputs from the stage and
+// writes m, v, the master and the rounded weights back into it.
+template <bool kMaster, uint32_t T, uint32_t CAP>
+__device__ __forceinline__ void stage_group(const StepArgs& p, const SegTable<CAP>& segs, Cursor& c, uint8_t* sp,
+                                            uint32_t g, uint64_t e0, float scale, const Hyper& h, uint32_t seed) {
+  using L = TmaStage<kMaster, T>;
+  const uint64_t gi = p.goff + e0 + 4u * g;
+  const uint2 graw = *reinterpret_cast<const uint2*>(sp + L::kGrads + 8u * g);
+  float4 m4 = *reinterpret_cast<const float4*>(sp + L::kM + 16u * g);
+  float4 v4 = *reinterpret_cast<const float4*>(sp + L::kV + 16u * g);
+  float w[kGroup];
+  if constexpr (kMaster) {
+    const float4 a = *reinterpret_cast<const float4*>(sp + L::kW + 16u * g);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(sp + L::kW + 8u * g);
+    w[0] = bf16_lo(a.x); w[1] = bf16_hi(a.x); w[2] = bf16_lo(a.y); w[3] = bf16_hi(a.y);
+  }
+  float wd[kGroup];
+  group_decay(c, segs, p, gi, wd);
+  const uint2 q = group_update(graw, m4, v4, w, wd, scale, h, gi, seed);
+  *reinterpret_cast<float4*>(sp + L::kM + 16u * g) = m4;
+  *reinterpret_cast<float4*>(sp + L::kV + 16u * g) = v4;
+  if constexpr (kMaster) {
+    *reinterpret_cast<float4*>(sp + L::kW + 16u * g) = make_float4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint2*>(sp + L::kGrads + 8u * g) = q;
+  } else {
+    *reinterpret_cast<uint2*>(sp + L::kW + 8u * g) = q;
+  }
+}
+
 }  // namespace mpk

@@ -464,6 +464,68 @@ def test_step_every_line_offset_of_the_vector_path(with_master):
         _compare(d, host, f"line offset {pad} elements")
 
 
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("with_master", [True, False])
+@pytest.mark.parametrize("extra,pad,tmax,goff", [(0, 0, 5000, 0), (2047, 4, 1 << 19, 0), (1, 60, 1200, 0),
+                                                 (777, 20, 60_000, 0), (1001, 8, 900, (1 << 32) - 700_003)])
+def test_step_tma_path(with_master, extra, pad, tmax, goff):
+    """Ranges of at least two 2048-element tiles per SM whose tiles start
+    16-B aligned in every array run the TMA-staged kernel (whole tiles loaded
+    and stored by bulk copies, updated in shared memory). Heads (the elements
+    before the gradients' next 128-B line, from the buffer's offset `pad`),
+    ragged tails, decay tables of under 32 and of hundreds of segments (the
+    two table sizes a launch carries) and a global range across index 2^32
+    must give the oracle's bits."""
+    n = 2 * _sms() * 2048 + 4096 + extra
+    tab, params, grads, master, m, v = _random_case(n, n + pad, 1, tmax)
+    if goff:
+        tab = [(0, goff, 1)] + [(o + goff, sz, dcy) for o, sz, dcy in tab]
+    lr, b1, b2, eps, wd, scale, t, seed = 2e-3, 0.9, 0.95, 1e-8, 0.1, 0.63, 4, 1234
+    d = dict(params=dev_u16(params, pad), grads=dev_u16(grads, pad), m=dev_f32(m, pad), v=dev_f32(v, pad),
+             master=dev_f32(master, pad) if with_master else None)
+    d_scale = torch.tensor([scale], dtype=torch.float32, device=DEV)
+    mp.mp_adamw_step(d["params"], d["grads"], d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=lr, beta1=b1,
+                     beta2=b2, eps=eps, weight_decay=wd, d_grad_scale=d_scale, t=t, seed=seed, global_offset=goff,
+                     n=n)
+    host = dict(params=params.copy(), master=master.copy() if with_master else None, m=m.copy(), v=v.copy())
+    assert oracle.adamw_step(host["params"], grads, host["master"], host["m"], host["v"], goff, tab, lr, b1, b2,
+                             eps, wd, f32(scale), t, seed) == 0
+    _compare(d, host, f"TMA path n={n} pad={pad}")
+
+
+@pytest.mark.parametrize("with_master", [True, False])
+def test_step_tma_path_many_steps_and_mixed_alignment(with_master):
+    """Eight steps in a row on one state (each step's results feed the next
+    through the staged tiles), then the same range with the weights offset
+    by 8 B against the gradients, which keeps the register path: both must
+    follow the oracle bit for bit."""
+    n = 2 * _sms() * 2048 + 3 * 2048 + 513
+    tab, params, grads, master, m, v = _random_case(n, 77, 1, 20_000)
+    host = dict(params=params.copy(), master=master.copy() if with_master else None, m=m.copy(), v=v.copy())
+    d = dict(params=dev_u16(params), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master) if with_master else None)
+    d_scale = torch.tensor([0.9], dtype=torch.float32, device=DEV)
+    rng = np.random.default_rng(5)
+    for t in range(1, 9):
+        g = bf16_from_f32(rng.standard_normal(n) * 1e-2)
+        mp.mp_adamw_step(d["params"], dev_u16(g), d["master"], d["m"], d["v"], mp.TensorTable(tab), lr=1e-3,
+                         beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, d_grad_scale=d_scale, t=t, seed=t)
+        assert oracle.adamw_step(host["params"], g, host["master"], host["m"], host["v"], 0, tab, 1e-3, 0.9, 0.95,
+                                 1e-8, 0.1, f32(0.9), t, t) == 0
+    _compare(d, host, "TMA path, 8 steps")
+    # weights 4 elements (8 B) off the gradients' alignment: bulk copies of the
+    # weights would start mid-16-B, so this range stays on the register path
+    host2 = dict(params=params.copy(), master=master.copy() if with_master else None, m=m.copy(), v=v.copy())
+    d2 = dict(params=dev_u16(params, 4), m=dev_f32(m), v=dev_f32(v), master=dev_f32(master) if with_master else None)
+    mp.mp_adamw_step(d2["params"], dev_u16(grads), d2["master"], d2["m"], d2["v"], mp.TensorTable(tab), lr=1e-3,
+                     beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, d_grad_scale=d_scale, t=1, seed=1)
+    assert oracle.adamw_step(host2["params"], grads, host2["master"], host2["m"], host2["v"], 0, tab, 1e-3, 0.9,
+                             0.95, 1e-8, 0.1, f32(0.9), 1, 1) == 0
+    _compare(d2, host2, "mixed alignment")
+
+
 @pytest.mark.parametrize("goff", [(1 << 32) - 3001, (1 << 32) - 3002, (1 << 32) - 3003, (1 << 32) - 3004])
 def test_step_global_offset_across_2_pow_32(goff):
     """A shard whose global range crosses index 2^32 from an offset that is
