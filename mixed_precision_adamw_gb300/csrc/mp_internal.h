@@ -98,12 +98,13 @@ cudaError_t launch_pdl_smem(void (*kernel)(Params...), unsigned grid, unsigned b
 }
 
 // Asks the GPU to keep the largest shared-memory carve-out on SMs that run
-// `kernel`. The TMA-staged step kernel needs most of an SM's shared memory;
-// an SM whose carve-out was set small by another kernel's blocks must drain
-// before it can take one of its blocks, so a persistent kernel beside it (the
-// host-gradient copy) or just before it (the norm) would otherwise serialise
-// with it. Once per kernel (`done` belongs to that kernel) and device; a hint,
-// so a failure is ignored.
+// `kernel`. The TMA-staged step kernel needs most of an SM's shared memory.
+// Measured on GB300: when the host-gradient copy (a persistent kernel beside
+// the step) or the norm (just before it in the stream) ran without this
+// preference, the step kernel's blocks waited for those kernels to leave the
+// SMs, and a pipelined step took the copy's time plus much of the update's.
+// Once per kernel (`done` belongs to that kernel) and device; a hint, so a
+// failure is ignored.
 template <typename... Params>
 void prefer_max_shared(void (*kernel)(Params...), std::atomic<bool> (&done)[64]) {
   int dev = 0;
