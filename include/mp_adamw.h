@@ -247,7 +247,14 @@ int mp_lr_at(const mp_lr_schedule_t* s, int64_t t, float* lr);
  *   seed        per-step rounding seed.
  *   d_status    int32[1], device, may be NULL; written only on that device-
  *               side error, and only while it holds 0 (the caller zeroes it
- *               and reads it after a sync).
+ *               and reads it after a sync). MP_ERR_CUDA there means a kernel
+ *               gave up waiting (one second) for its own staged copies, which
+ *               only a fault of the GPU or of the library can cause.
+ * Launches: ranges of at least two tiles per SM (tiles of 2,304 elements with
+ * master, 3,328 without) whose arrays are 16-B aligned where the tiles start
+ * run a kernel that stages whole tiles through shared memory with the TMA
+ * engine (one block per SM, 129 KB or 200 KB of shared memory); others run a
+ * register-only kernel. Both give the same bits.
  * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_TABLE, MP_ERR_RANGE, MP_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 int mp_adamw_step(uint16_t* params, const uint16_t* grads, float* master,

@@ -24,7 +24,9 @@ constexpr uint32_t kSegCapLarge = 1024;
 // elements the persistent blocks drift apart and DRAM streams slower; on
 // GB300, launches of ~200M elements (1 ms) ran 1 % faster over GPT-2 1.5B and
 // Llama-3-8B parameter sets than one launch, and much shorter ones lost
-// time at the launch boundaries.
+// time at the launch boundaries. The TMA-staged kernel agrees: the 8B set's
+// update took 33.3 ms in 40 launches, 33.4 in 20 or 60, 33.5 in 10 or 80 and
+// 34.2 ms in one.
 constexpr uint64_t kMaxLaunchElems = uint64_t{3} << 26;  // 201,326,592
 
 struct StepArgs {
