@@ -601,7 +601,7 @@ def measure_stream_probes(st, g, N, stream, peak):
                                                     "frac": round(STEP_BYTES_MASTER * n / ms / 1e6 / peak, 4),
                                                     "ms": round(ms, 5)}
     # the same streams staged through shared memory by TMA bulk copies
-    for bps, stages, hint in ((1, 4, 1), (1, 7, 1), (1, 7, 0), (2, 3, 1)):
+    for bps, stages, hint in ((1, 3, 1), (1, 3, 0), (1, 4, 1), (1, 7, 1), (2, 2, 1), (2, 3, 1)):
         def run_bulk():
             for a in range(0, n, chunk):
                 b = min(n, a + chunk)
