@@ -23,6 +23,7 @@
 #include "mp_device.cuh"
 #include "mp_internal.h"
 #include "mp_norm.cuh"
+#include "mp_tma.cuh"
 
 namespace mpk {
 namespace {
@@ -38,6 +39,101 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
   pdl_enter();
   const double S = norm_block_partial<kCopy>(grads, n, vec, copy_out, blockIdx.x, gridDim.x, sh);
   if (threadIdx.x == 0) partials[blockIdx.x] = S;
+}
+
+// Level 1 with the gradients staged through shared memory by the TMA engine,
+// for 16-B aligned device gradients: the element mapping and the order of
+// every addition are norm_partial_kernel's, so each partial has the same bits.
+// Block b's vectors of iteration j, b*256 + j*nblocks*256 + t for t < 256,
+// are one contiguous 4 KB piece. Thread 0 has piece j + kNormTmaStages - 1
+// loaded by a bulk copy into a ring of stages while the block adds piece j
+// (thread t the vector t); a stage is loaded again once every warp has read
+// it (an mbarrier per stage each way). The loads do not pass through L1, so
+// the kernel keeps its rate with most of the SM's memory as shared memory,
+// where the TMA-staged step kernel must run beside or after it. Every wait
+// gives up after one second; a block that gave up writes a NaN partial, so
+// the norm and scale come out NaN and the step refuses to run.
+constexpr uint32_t kNormTmaStages = 3;
+constexpr uint32_t kNormPiecesPerStage = 4;
+constexpr uint32_t kNormPieceBytes = kThreads * 16;
+constexpr uint32_t kNormStageBytes = kNormPiecesPerStage * kNormPieceBytes;
+constexpr size_t kNormTmaSmem = kNormTmaStages * kNormStageBytes + 16 * kNormTmaStages;
+
+__global__ void __launch_bounds__(kThreads)
+norm_partial_tma_kernel(const uint16_t* __restrict__ grads, uint64_t n, double* __restrict__ partials) {
+  __shared__ double sh[kThreads / 32 + 1];
+  __shared__ int gave_up;
+  extern __shared__ __align__(128) uint8_t ring[];
+  pdl_enter();
+  constexpr uint32_t S = kNormTmaStages, G = kNormPiecesPerStage;
+  const uint32_t base = smem_u32(ring), full = base + S * kNormStageBytes, done = full + 8 * S;
+  const uint64_t nvec = n / 8, stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+  const uint64_t first = static_cast<uint64_t>(blockIdx.x) * kThreads;  // vector 0 of piece 0
+  const uint64_t pieces = first < nvec ? (nvec - first - 1) / stride + 1 : 0;
+  const uint64_t groups = (pieces + G - 1) / G;  // stage loads: pieces G*q .. G*q + G - 1
+  if (threadIdx.x == 0) {
+    gave_up = 0;
+    for (uint32_t i = 0; i < S; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(done + 8 * i, kThreads / 32);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const uint4* g4 = reinterpret_cast<const uint4*>(grads);
+  uint64_t policy = 0, issued = 0;
+  auto load = [&](uint64_t q) {
+    const uint32_t st = static_cast<uint32_t>(q % S);
+    const uint64_t p1 = (q + 1) * G < pieces ? (q + 1) * G : pieces;
+    uint32_t total = 0;
+    for (uint64_t p = q * G; p < p1; ++p) {
+      const uint64_t left = nvec - (first + p * stride);
+      total += static_cast<uint32_t>((left < kThreads ? left : kThreads) * 16);
+    }
+    mbar_expect_tx(full + 8 * st, total);
+    for (uint64_t p = q * G; p < p1; ++p) {
+      const uint64_t v0 = first + p * stride, left = nvec - v0;
+      bulk_load(base + st * kNormStageBytes + static_cast<uint32_t>(p - q * G) * kNormPieceBytes, g4 + v0,
+                static_cast<uint32_t>((left < kThreads ? left : kThreads) * 16), full + 8 * st, policy);
+    }
+  };
+  bool producing = threadIdx.x == 0;
+  if (producing) {
+    policy = l2_evict_first();
+    for (; issued < groups && issued + 1 < S; ++issued) load(issued);
+  }
+  float s = 0.0f, c = 0.0f;
+  uint64_t q = 0;
+  for (; q < groups; ++q) {
+    const uint32_t st = static_cast<uint32_t>(q % S);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + 8 * st, static_cast<uint32_t>((q / S) & 1)))) {
+      if ((threadIdx.x & 31) == 0) atomicExch(&gave_up, 1);
+      break;
+    }
+    const uint8_t* sp = ring + st * kNormStageBytes + 16u * threadIdx.x;
+#pragma unroll
+    for (uint32_t g = 0; g < G; ++g) {
+      const uint64_t p = q * G + g;
+      if (p < pieces && first + p * stride + threadIdx.x < nvec)
+        acc(s, c, sumsq8(*reinterpret_cast<const uint4*>(sp + g * kNormPieceBytes)));
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(done + 8 * st);
+    if (producing && issued < groups) {
+      // group `issued` (q + S - 1) goes into the stage that group q - 1 used
+      if (q >= 1 && !mbar_wait(done + 8 * ((q - 1) % S), static_cast<uint32_t>(((q - 1) / S) & 1))) {
+        atomicExch(&gave_up, 1);
+        producing = false;
+      } else {
+        load(issued++);
+      }
+    }
+  }
+  if (threadIdx.x == 0)  // loads this thread issued and did not see land: bounded waits
+    for (uint64_t p = q; p < issued; ++p)
+      mbar_wait(full + 8 * static_cast<uint32_t>(p % S), static_cast<uint32_t>((p / S) & 1));
+  const double P = norm_block_finish<false>(grads, n, 1, nullptr, blockIdx.x, gridDim.x, sh, s, c);
+  if (threadIdx.x == 0) partials[blockIdx.x] = gave_up ? __longlong_as_double(0x7FF8000000000000ll) : P;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -98,9 +194,29 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
   // pipelined step 24-25 ms instead of 19.5 ms). The cost: any explicit
   // carve-out, from 25 % to the largest, runs this kernel alone 15 % slower.
   static std::atomic<bool> carve_plain[64], carve_copy[64], carve_finalize[64];
+  prefer_max_shared(norm_finalize_kernel, carve_finalize);
+  // Aligned device gradients with at least two pieces per block: the
+  // TMA-staged kernel (the same partials, bit for bit).
+  const uint64_t stride = static_cast<uint64_t>(nblocks) * kThreads;
+  if (vec && copy_out == nullptr && n / 8 >= 2 * stride) {
+    static std::atomic<bool> smem_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !smem_set[dev].load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(norm_partial_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kNormTmaSmem));
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) smem_set[dev].store(true, std::memory_order_relaxed);
+    }
+    e = launch_pdl_smem(norm_partial_tma_kernel, static_cast<unsigned>(nblocks), kThreads,
+                        kNormTmaSmem, stream, grads, n, partials);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(norm_finalize_kernel, 1u, kThreads, stream, static_cast<const double*>(partials), nblocks,
+                      clip, d_norm, d_scale, d_sumsq, c);
+  }
   if (copy_out == nullptr) prefer_max_shared(norm_partial_kernel<false>, carve_plain);
   else prefer_max_shared(norm_partial_kernel<true>, carve_copy);
-  prefer_max_shared(norm_finalize_kernel, carve_finalize);
   cudaError_t e = copy_out == nullptr
                       ? launch_pdl(norm_partial_kernel<false>, static_cast<unsigned>(nblocks), kThreads, stream,
                                    grads, n, vec ? 1 : 0, partials, copy_out)

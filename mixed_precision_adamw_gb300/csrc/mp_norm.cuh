@@ -78,6 +78,11 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
 // its order are the same as without the copy. Every thread of the block
 // calls it and receives the block's partial.
 template <bool kCopy>
+__device__ __forceinline__ double norm_block_finish(const uint16_t* __restrict__ grads, uint64_t n, int vec,
+                                                    uint16_t* __restrict__ copy_out, uint32_t block,
+                                                    uint32_t nblocks, double* sh, float s, float c);
+
+template <bool kCopy>
 __device__ __forceinline__ double norm_block_partial(const uint16_t* __restrict__ grads, uint64_t n, int vec,
                                                      uint16_t* __restrict__ copy_out, uint32_t block,
                                                      uint32_t nblocks, double* sh) {
@@ -105,6 +110,21 @@ __device__ __forceinline__ double norm_block_partial(const uint16_t* __restrict_
     if (kCopy) c4[k] = w;
     acc(s, c, sumsq8(w));
   }
+  return norm_block_finish<kCopy>(grads, n, vec, copy_out, block, nblocks, sh, s, c);
+}
+
+// The rest of a norm block's partial after its 8-element vectors have been
+// added into (s, c) in the thread's order: the scalar tail, the fixed block
+// sum and the fp64 recomputation. Every thread of the block calls it.
+template <bool kCopy>
+__device__ __forceinline__ double norm_block_finish(const uint16_t* __restrict__ grads, uint64_t n, int vec,
+                                                    uint16_t* __restrict__ copy_out, uint32_t block,
+                                                    uint32_t nblocks, double* sh, float s, float c) {
+  const uint4* g4 = reinterpret_cast<const uint4*>(grads);
+  const uint64_t nvec = vec ? n / 8 : 0;
+  const uint64_t stride = static_cast<uint64_t>(nblocks) * kThreads;
+  const uint64_t k0 = static_cast<uint64_t>(block) * kThreads + threadIdx.x;
+  uint64_t k;
   for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
     const uint16_t h = grads[i];
     if (kCopy) copy_out[i] = h;

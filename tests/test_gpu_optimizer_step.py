@@ -131,11 +131,52 @@ def test_host_gradients_unaligned_and_ragged(host_off, dev_off, n):
         assert _same(a[k], b[k]), k
 
 
+def _staged_norm_threshold():
+    """Elements from which aligned device gradients take the TMA-staged norm
+    kernel: two 4 KB pieces (256 vectors of 8) per norm block, 4 blocks per SM."""
+    return 2 * 4 * torch.cuda.get_device_properties(0).multi_processor_count * 256 * 8
+
+
+@pytest.mark.parametrize("extra", [-8, 0, 8 * 257 + 5, 2_509_635, 37_509_633])
+def test_staged_norm_partials_equal_the_register_norm_bit_for_bit(extra):
+    """Device gradients past the threshold go through the TMA-staged norm
+    kernel; pinned host gradients always through the register kernel, which
+    reads them over the link. Both add every square in the same order, so
+    every per-block partial left in the workspace must be the same fp64 bits,
+    and so must the norm and the updated state."""
+    n = _staged_norm_threshold() + extra
+    gen = torch.Generator().manual_seed(n)
+    g_cpu = (torch.randn(n, generator=gen) * 1e-2).to(torch.bfloat16)
+    host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    host.copy_(g_cpu)
+    master = (torch.randn(n, generator=gen) * 0.05).cuda()
+    st = dict(params=master.to(torch.bfloat16), master=master, m=torch.zeros_like(master), v=torch.zeros_like(master))
+    tab = [(0, n // 3, 1), (n // 3, n - n // 3, 0)]
+    kw = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, clip=1.0)
+    a = {k: x.clone() for k, x in st.items()}
+    b = {k: x.clone() for k, x in st.items()}
+    opt_a, opt_b = mp.Optimizer(tab, **kw), mp.Optimizer(tab, **kw)
+    opt_a.workspace.zero_()
+    opt_b.workspace.fill_(0x5A)
+    opt_a.step(a["params"], g_cpu.cuda(), a["master"], a["m"], a["v"], 2, 9)
+    landing = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    opt_b.step(b["params"], landing, b["master"], b["m"], b["v"], 2, 9, host_grads=host)
+    torch.cuda.synchronize()
+    nb = 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    wa = opt_a.workspace[: nb * 8].view(torch.int64)
+    wb = opt_b.workspace[: nb * 8].view(torch.int64)
+    assert torch.equal(wa, wb)
+    assert opt_a.d_norm.item() == opt_b.d_norm.item()
+    for k in a:
+        assert _same(a[k], b[k]), k
+
+
 @pytest.mark.parametrize("scale", [1e-30, 1e25])
-def test_host_gradients_extreme_values_take_the_fp64_path(scale):
+@pytest.mark.parametrize("n", [3 * 2048 * 152 + 11, 3 * (1 << 20) + 11])
+def test_host_gradients_extreme_values_take_the_fp64_path(scale, n):
     """Blocks whose fp32 squares underflow or overflow recompute in fp64 from
-    the device copy; the norm must match the device-gradient path."""
-    n = 3 * 2048 * 152 + 11
+    the device copy; the norm must match the device-gradient path (which,
+    at the larger size, is the TMA-staged norm kernel)."""
     g_cpu = (torch.randn(n, generator=torch.Generator().manual_seed(1)) * scale).to(torch.bfloat16)
     host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
     host.copy_(g_cpu)
