@@ -8,7 +8,9 @@
 // bf16 gradients in fp32 (exact for |g| in [2^-63, 2^64)), adds each 8-element
 // vector as a pairwise tree and accumulates the vector sums with Fast2Sum
 // compensation; the threads of a block are reduced in fp64 by a fixed
-// warp-shuffle tree and a fixed shared-memory pass. A block whose fp32 result
+// warp-shuffle tree and a fixed shared-memory pass. For long aligned device
+// gradients norm_partial_tma_kernel does the same additions in the same
+// order on vectors that the TMA engine stages in shared memory. A block whose fp32 result
 // is non-finite or below 2^-60 (possible overflow or underflow of the fp32
 // squares) recomputes its share in fp64. Level 2 (norm_finalize_kernel, one
 // block) adds the per-block partials in a fixed order, takes the square root
@@ -45,12 +47,17 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
 // for 16-B aligned device gradients: the element mapping and the order of
 // every addition are norm_partial_kernel's, so each partial has the same bits.
 // Block b's vectors of iteration j, b*256 + j*nblocks*256 + t for t < 256,
-// are one contiguous 4 KB piece. Thread 0 has piece j + kNormTmaStages - 1
-// loaded by a bulk copy into a ring of stages while the block adds piece j
-// (thread t the vector t); a stage is loaded again once every warp has read
-// it (an mbarrier per stage each way). The loads do not pass through L1, so
-// the kernel keeps its rate with most of the SM's memory as shared memory,
-// where the TMA-staged step kernel must run beside or after it. Every wait
+// are one contiguous 4 KB piece. Thread 0 has groups of kNormPiecesPerStage
+// pieces loaded by bulk copies into a ring of kNormTmaStages stages while the
+// block adds the pieces of an earlier group in order (thread t the vector t
+// of each); a stage is loaded again once every warp has read it (an mbarrier
+// per stage each way). Measured on GB300 (Llama-3-8B gradients, 16 GB): 4
+// pieces x 3 stages 2.46 ms; 3 x 4 2.50; 6 x 2 2.65; 2 x 6 3.09; 1 x 8 2.90;
+// the register kernel 2.55 ms in the same shared-memory configuration. The
+// loads do not pass through L1, so the kernel keeps its rate with most of the
+// SM's memory as shared memory, where the TMA-staged step kernel must run
+// beside or after it (with it the norm -> update boundary of a step costs
+// nothing measurable; with the register kernel it cost 0.3 ms). Every wait
 // gives up after one second; a block that gave up writes a NaN partial, so
 // the norm and scale come out NaN and the step refuses to run.
 constexpr uint32_t kNormTmaStages = 3;
@@ -189,14 +196,16 @@ cudaError_t launch_norm(const uint16_t* grads, uint64_t n, bool vec, double* par
                         float clip, float* d_norm, float* d_scale, double* d_sumsq, cudaStream_t stream,
                         uint16_t* copy_out, const StepClock* clock) {
   const StepClock c = clock != nullptr ? *clock : StepClock{nullptr, nullptr, 0, nullptr};
-  // Beside the host-gradient copy the norm would otherwise move SMs to a
-  // configuration the step kernel cannot share (measured on GB300: a 2B-param
-  // pipelined step 24-25 ms instead of 19.5 ms). The cost: any explicit
-  // carve-out, from 25 % to the largest, runs this kernel alone 15 % slower.
+  // Aligned device gradients with at least two pieces per block take the
+  // TMA-staged kernel (the same partials, bit for bit), which keeps its rate
+  // in the large shared-memory configuration the TMA-staged step kernel
+  // needs. The other kernels here ask for that configuration too, so that the
+  // step kernel can share SMs with them. Measured on GB300: without it a
+  // pipelined 2B-param step took 24-25 ms instead of 19.5 ms; with it (any
+  // explicit carve-out from 25 % up) the register partial kernel runs alone
+  // about 15 % slower.
   static std::atomic<bool> carve_plain[64], carve_copy[64], carve_finalize[64];
   prefer_max_shared(norm_finalize_kernel, carve_finalize);
-  // Aligned device gradients with at least two pieces per block: the
-  // TMA-staged kernel (the same partials, bit for bit).
   const uint64_t stride = static_cast<uint64_t>(nblocks) * kThreads;
   if (vec && copy_out == nullptr && n / 8 >= 2 * stride) {
     static std::atomic<bool> smem_set[64];
