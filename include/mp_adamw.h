@@ -300,6 +300,10 @@ int mp_step_launches(uint64_t global_offset, uint64_t n, const mp_tensor_t* tabl
  *   out[i] = SR(in[i], global_offset + i, seed)  for i < n   (rule above)
  *
  *   out   bf16[n], device, written.   in   fp32[n], device, read only.
+ * Launches: with both arrays 16-B aligned and n at least 128 tiles of 6,144
+ * elements per SM, a kernel that stages whole tiles through shared memory
+ * with the TMA engine (one block per SM, 221 KB of shared memory); otherwise
+ * a register-only kernel. Both give the same bits.
  * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 int mp_stochastic_round(uint16_t* out, const float* in,
@@ -337,6 +341,10 @@ int mp_stochastic_round_fp16(uint16_t* out, const float* in,
  *
  *   acc     bf16[n], device, read and written in place.
  *   delta   fp32[n], device, read only; must not overlap acc.
+ * Launches: with both arrays 16-B aligned and n at least 80 tiles of 4,096
+ * elements per SM, a kernel that stages whole tiles through shared memory
+ * with the TMA engine (one block per SM, 147 KB of shared memory); otherwise
+ * a register-only kernel. Both give the same bits.
  * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE, MP_ERR_CUDA.
  * ------------------------------------------------------------------------- */
 int mp_accumulate_sr(uint16_t* acc, const float* delta,

@@ -8,12 +8,17 @@
 // keyed on the global element index, the rebuild needs no launch-geometry
 // alignment: any grid gives the same bits. 6 B of HBM traffic per element;
 // at that ratio the draw's integer work (about 19 operations per element)
-// keeps the integer ALU pipe nearly saturated, so these kernels run a little
-// below the memory bound. The same section has the rounding write the
-// encoder's embedding gradients: a bf16 gradient plus an fp32 contribution,
-// rounded back (8 B per element).
+// keeps the integer ALU pipe busy, so the register kernels run a little below
+// the memory bound; long aligned ranges of the bf16 rounding and of the
+// accumulation take TMA-staged kernels (below), which hide the memory latency
+// from the warps. The same section has the rounding write the encoder's
+// embedding gradients: a bf16 gradient plus an fp32 contribution, rounded
+// back (8 B per element).
+#include <atomic>
+
 #include "mp_device.cuh"
 #include "mp_internal.h"
+#include "mp_tma.cuh"
 
 namespace mpk {
 namespace {
@@ -186,6 +191,162 @@ accumulate_scalar_kernel(uint16_t* __restrict__ acc, const float* __restrict__ d
         sr_bf16_c(__fadd_rn(bf16_to_f32(acc[i]), delta[i]), draw16_complement(noise_pos(goff + i), seed)));
 }
 
+// ---- TMA-staged rounding (long aligned ranges) --------------------------------
+// The bf16 rounding and accumulate-and-round kernels above on tiles that the
+// TMA engine stages in shared memory, as the step kernel's TMA path does: one
+// block per SM; thread 0 has whole tiles of the inputs loaded by bulk copies
+// into a ring of stages and, once the consumer warps have rounded a tile, the
+// output stored by bulk copies. Consumer thread c rounds the 4-element groups
+// c and c + consumers of a tile with the code of the register kernels (the
+// same draws and bits). Every wait gives up after one second; nothing then
+// reports it, but the outputs of the tiles not stored stay as they were.
+// Measured on GB300 (201M elements, interleaved builds): bf16 rounding 6.44
+// TB/s at 24 consumer warps x 6 stages (16 x 6: 6.03, 28 x 5: 6.42, 16 x 4:
+// 5.35) against 6.25 for sr_vec_kernel; accumulate-and-round 6.83 at 16 x 6
+// (12 x 8: 6.85, 24 x 4: 6.72, 8 x 4: 4.82) against 6.26-6.32 for
+// accumulate_vec_kernel. The fp16 rounding stays on its register kernel:
+// bound by the integer pipe, it ran 5.53-5.58 staged against 5.58-5.60.
+enum class RoundKind { kBf16, kAccumulate };
+
+template <RoundKind K>
+struct RoundTma {
+  static constexpr int kConsumerWarps = K == RoundKind::kAccumulate ? 16 : 24;
+  static constexpr uint32_t kStages = 6;
+  // Ranges shorter than this many tiles per SM keep the register kernel: the
+  // pipeline's fill and drain cost more than the staging saves. Measured on
+  // GB300 against the register kernels (3 interleaved runs each): bf16
+  // rounding -17 % at 16.8M elements (18 tiles per SM), -10 % at 33.6M,
+  // -1.5 % at 67.1M (72), +3 % at 201M (215); accumulate -16 % at 16.8M
+  // (27), -13 % at 33.6M (54), +2.3 % at 67.1M (108), +8 % at 201M.
+  static constexpr uint64_t kMinTilesPerSm = K == RoundKind::kAccumulate ? 80 : 128;
+  static constexpr int kConsumers = 32 * kConsumerWarps;
+  static constexpr int kThreads = 32 + kConsumers;
+  static constexpr uint32_t kTileElems = static_cast<uint32_t>(kConsumers) * 2 * kGroup;
+  // Stage layout. Rounding: the fp32 inputs, then the bf16 outputs.
+  // Accumulate: the bf16 accumulators (rounded in place), then the fp32
+  // contributions.
+  static constexpr uint32_t kIn = K == RoundKind::kAccumulate ? kTileElems * 2 : 0;      // fp32
+  static constexpr uint32_t kOut = K == RoundKind::kAccumulate ? 0 : kTileElems * 4;     // 16-bit
+  static constexpr uint32_t kBytes = kTileElems * 6;
+  // bytes the loads of one tile bring (the barrier's expected count)
+  static constexpr uint32_t kLoadBytes = K == RoundKind::kAccumulate ? kTileElems * 6 : kTileElems * 4;
+  static constexpr size_t kSmemBytes = kStages * kBytes + 16 * kStages;
+};
+
+template <RoundKind K>
+__global__ void __launch_bounds__(RoundTma<K>::kThreads, 1)
+round_tma_kernel(uint16_t* __restrict__ out, const float* __restrict__ in, uint64_t goff, uint64_t n,
+                 uint32_t seed) {
+  pdl_enter();
+  using C = RoundTma<K>;
+  constexpr uint32_t S = C::kStages, T = C::kTileElems;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t base = smem_u32(smem), full = base + S * C::kBytes, done = full + 8 * S;
+  if (threadIdx.x == 0) {
+    for (uint32_t i = 0; i < S; ++i) {
+      mbar_init(full + 8 * i, 1);
+      mbar_init(done + 8 * i, C::kConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const uint64_t ntiles = n / T;
+  const uint64_t mine = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto elem = [&](uint64_t k) { return (blockIdx.x + k * gridDim.x) * static_cast<uint64_t>(T); };
+
+  if (threadIdx.x < 32) {  // the producer
+    if (threadIdx.x != 0) return;
+    const uint64_t pol = l2_evict_first();
+    auto load = [&](uint64_t k) {
+      const uint32_t st = static_cast<uint32_t>(k % S), bar = full + 8 * st, sp = base + st * C::kBytes;
+      const uint64_t e = elem(k);
+      mbar_expect_tx(bar, C::kLoadBytes);
+      if constexpr (K == RoundKind::kAccumulate) bulk_load(sp, out + e, T * 2, bar, pol);
+      bulk_load(sp + C::kIn, in + e, T * 4, bar, pol);
+    };
+    uint64_t issued = 0, k = 0;
+    for (; issued < mine && issued + 1 < S; ++issued) load(issued);
+    bool ok = true;
+    for (; k < mine; ++k) {
+      const uint32_t st = static_cast<uint32_t>(k % S);
+      if (!mbar_wait(done + 8 * st, static_cast<uint32_t>((k / S) & 1))) {
+        ok = false;
+        break;
+      }
+      bulk_store(out + elem(k), base + st * C::kBytes + C::kOut, T * 2, pol);
+      bulk_commit();
+      if (issued < mine) {
+        bulk_wait_read<1>();
+        load(issued++);
+      }
+    }
+    if (!ok)
+      for (uint64_t j = k; j < issued; ++j)
+        mbar_wait(full + 8 * static_cast<uint32_t>(j % S), static_cast<uint32_t>((j / S) & 1));
+    bulk_wait_all();
+    return;
+  }
+
+  const uint32_t ci = threadIdx.x - 32;
+  for (uint64_t k = 0; k < mine; ++k) {
+    const uint32_t st = static_cast<uint32_t>(k % S);
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full + 8 * st, static_cast<uint32_t>((k / S) & 1)))) break;
+    uint8_t* sp = smem + st * C::kBytes;
+    const uint64_t e0 = goff + elem(k) + 4u * ci, e1 = e0 + 4u * C::kConsumers;
+    const float4 a = *reinterpret_cast<const float4*>(sp + C::kIn + 16u * ci);
+    const float4 b = *reinterpret_cast<const float4*>(sp + C::kIn + 16u * (ci + C::kConsumers));
+    uint2 qa, qb;
+    if constexpr (K == RoundKind::kBf16) {
+      sr_pack8(a, b, e0, e1, seed, qa, qb);
+    } else {
+      const uint2 a0 = *reinterpret_cast<const uint2*>(sp + 8u * ci);
+      const uint2 a1 = *reinterpret_cast<const uint2*>(sp + 8u * (ci + C::kConsumers));
+      const float4 s0 = make_float4(__fadd_rn(bf16_lo(a0.x), a.x), __fadd_rn(bf16_hi(a0.x), a.y),
+                                    __fadd_rn(bf16_lo(a0.y), a.z), __fadd_rn(bf16_hi(a0.y), a.w));
+      const float4 s1 = make_float4(__fadd_rn(bf16_lo(a1.x), b.x), __fadd_rn(bf16_hi(a1.x), b.y),
+                                    __fadd_rn(bf16_lo(a1.y), b.z), __fadd_rn(bf16_hi(a1.y), b.w));
+      sr_pack8(s0, s1, e0, e1, seed, qa, qb);
+    }
+    *reinterpret_cast<uint2*>(sp + C::kOut + 8u * ci) = qa;
+    *reinterpret_cast<uint2*>(sp + C::kOut + 8u * (ci + C::kConsumers)) = qb;
+    fence_to_bulk();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(done + 8 * st);
+  }
+  // ragged tail (< T elements), one element per thread
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * C::kConsumers;
+  for (uint64_t i = ntiles * T + static_cast<uint64_t>(blockIdx.x) * C::kConsumers + ci; i < n; i += stride) {
+    const uint32_t d = draw16_complement(noise_pos(goff + i), seed);
+    if constexpr (K == RoundKind::kBf16) out[i] = static_cast<uint16_t>(sr_bf16_c(in[i], d));
+    else out[i] = static_cast<uint16_t>(sr_bf16_c(__fadd_rn(bf16_to_f32(out[i]), in[i]), d));
+  }
+}
+
+// Launches round_tma_kernel<K> when the range holds at least kMinTilesPerSm
+// tiles per SM and both arrays are 16-B aligned (so every tile starts
+// aligned); false when it does not apply.
+template <RoundKind K>
+bool launch_round_tma(uint16_t* out, const float* in, uint64_t goff, uint64_t n, uint32_t seed,
+                      const DeviceInfo& dev, cudaStream_t stream, cudaError_t* err) {
+  using C = RoundTma<K>;
+  if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(in) % 16 ||
+      n / C::kTileElems < C::kMinTilesPerSm * static_cast<uint64_t>(dev.sms))
+    return false;
+  static std::atomic<bool> smem_set[64];
+  if (dev.device < 0 || dev.device >= 64 || !smem_set[dev.device].load(std::memory_order_relaxed)) {
+    const cudaError_t e = cudaFuncSetAttribute(round_tma_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) {
+      *err = e;
+      return true;
+    }
+    if (dev.device >= 0 && dev.device < 64) smem_set[dev.device].store(true, std::memory_order_relaxed);
+  }
+  *err = launch_pdl_smem(round_tma_kernel<K>, static_cast<unsigned>(dev.sms), C::kThreads, C::kSmemBytes, stream,
+                         out, in, goff, n, seed);
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads)
 noise_kernel(uint32_t* __restrict__ out, uint64_t first, uint64_t n, uint32_t seed) {
   pdl_enter();
@@ -206,6 +367,8 @@ unsigned grid_for(uint64_t units, const DeviceInfo& dev) {
 
 cudaError_t launch_sr(uint16_t* out, const float* in, uint64_t goff, uint64_t n, uint32_t seed, bool vec,
                       const DeviceInfo& dev, cudaStream_t stream) {
+  cudaError_t e;
+  if (vec && launch_round_tma<RoundKind::kBf16>(out, in, goff, n, seed, dev, stream, &e)) return e;
   if (vec) {
     const uint64_t ntiles = n / kTile;
     const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);
@@ -226,6 +389,8 @@ cudaError_t launch_sr_fp16(uint16_t* out, const float* in, uint64_t goff, uint64
 
 cudaError_t launch_accumulate_sr(uint16_t* acc, const float* delta, uint64_t goff, uint64_t n, uint32_t seed,
                                  bool vec, const DeviceInfo& dev, cudaStream_t stream) {
+  cudaError_t e;
+  if (vec && launch_round_tma<RoundKind::kAccumulate>(acc, delta, goff, n, seed, dev, stream, &e)) return e;
   if (vec) {
     const uint64_t ntiles = n / kTile;
     const unsigned blocks = ntiles ? grid_for(ntiles * kThreads, dev) : grid_for(n, dev);

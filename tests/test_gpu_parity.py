@@ -92,7 +92,9 @@ def _special_f32(n, rng):
     (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000),
     # vector path crossing 2^32 inside a 4-element group (offset not a multiple of 4)
     (2048 * 7 + 5, 0, 0, (1 << 32) - 5001), (2048 * 7 + 5, 0, 0, (1 << 32) - 5002),
-    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), (2048 * 7 + 5, 0, 0, (3 << 32) - 1)])
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), (2048 * 7 + 5, 0, 0, (3 << 32) - 1),
+    # longer aligned ranges, with a ragged tail, across 2^32, and an 8-B aligned output
+    (1_249_283, 0, 0, (1 << 32) - 600_001), ((1 << 22) + 3, 0, 0, 123), ((1 << 22) + 3, 0, 4, 99)])
 def test_stochastic_round_bit_exact(n, pad_in, pad_out, goff):
     rng = np.random.default_rng(n + pad_in)
     x = _special_f32(n, rng) if n > 2000 else rng.standard_normal(n).astype(np.float32)
@@ -103,10 +105,59 @@ def test_stochastic_round_bit_exact(n, pad_in, pad_out, goff):
     assert_bit_equal(to_np_u16(out), oracle.stochastic_round(x, goff, seed), "sr")
 
 
+def _long_round_n(tile, tiles_per_sm, extra):
+    """A length just past the TMA-staged rounding kernels' minimum (tiles per
+    SM of `tile` elements), with a ragged tail."""
+    return tiles_per_sm * torch.cuda.get_device_properties(0).multi_processor_count * tile + extra
+
+
+def _long_f32(n, rng):
+    """Weight-like and wide-range values with the special values sprinkled in."""
+    x = rng.standard_normal(n, dtype=np.float32)
+    x[: n // 2] *= np.float32(0.02)
+    with np.errstate(over="ignore"):
+        x[n // 2:] *= np.exp2(rng.integers(-140, 127, n - n // 2)).astype(np.float32)
+    sp = _special_f32(4096, rng)
+    idx = rng.integers(0, n, sp.size)
+    x[idx] = sp
+    return x
+
+
+@pytest.mark.parametrize("goff", [0, (1 << 32) - 60_000_001])
+def test_stochastic_round_long_range_tma_bit_exact(goff):
+    """A range long enough for the TMA-staged bf16 rounding kernel (128 tiles
+    of 6,144 elements per SM, plus a ragged tail), across index 2^32 in one
+    case: every element bit-exact against the oracle."""
+    n = _long_round_n(6144, 128, 12_345)
+    rng = np.random.default_rng(77)
+    x = _long_f32(n, rng)
+    out = torch.empty(n, dtype=torch.int16, device=DEV)
+    mp.mp_stochastic_round(out, dev_f32(x), 0xB16, global_offset=goff)
+    assert_bit_equal(to_np_u16(out), oracle.stochastic_round(x, goff, 0xB16), "sr long range")
+
+
+@pytest.mark.parametrize("goff", [0, (1 << 32) - 25_000_003])
+def test_accumulate_sr_long_range_tma_bit_exact(goff):
+    """A range long enough for the TMA-staged accumulate-and-round kernel (80
+    tiles of 4,096 elements per SM, plus a ragged tail), across index 2^32 in
+    one case: every accumulator bit-exact against the oracle."""
+    n = _long_round_n(4096, 80, 777)
+    rng = np.random.default_rng(78)
+    acc0 = bf16_from_f32(rng.standard_normal(n, dtype=np.float32) * np.float32(0.02))
+    acc0[rng.integers(0, n, 8)] = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x7F7F, 0xFF7F, 0x0001],
+                                           np.uint16)
+    delta = _long_f32(n, rng)
+    acc = dev_u16(acc0)
+    mp.mp_accumulate_sr(acc, dev_f32(delta), 0xACC2, global_offset=goff)
+    ref = acc0.copy()
+    oracle.accumulate_sr(ref, delta, goff, 0xACC2)
+    assert_bit_equal(to_np_u16(acc), ref, "accumulate_sr long range")
+
+
 @pytest.mark.parametrize("n,pad_acc,pad_delta,goff", [
     (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32), (1, 0, 0, 5),
     (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000), (2048 * 7 + 5, 0, 0, (1 << 32) - 5001),
-    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), ((1 << 22) + 3, 0, 0, 123)])
+    (2048 * 7 + 5, 0, 0, (1 << 32) - 5003), ((1 << 22) + 3, 0, 0, 123), (1_249_283, 0, 0, (1 << 32) - 600_001)])
 def test_accumulate_sr_bit_exact(n, pad_acc, pad_delta, goff):
     """acc = SR((float)acc + delta): special values on both sides (NaN, Inf,
     signed zeros, subnormals, the largest finite values), vector and scalar
@@ -152,7 +203,7 @@ def _fp16_cases(n, rng):
     (2048 * 7 + 5, 0, 0, 0), (2048 * 7 + 5, 1, 0, 17), (2048 * 7 + 5, 0, 1, 1 << 32),
     (1, 0, 0, 5), (2047, 0, 0, 0), (300001, 3, 2, (1 << 32) - 150000),
     (2048 * 7 + 5, 0, 0, (1 << 32) - 5001), (2048 * 7 + 5, 0, 0, (1 << 32) - 5003),
-    ((1 << 22) + 3, 0, 0, 123)])
+    ((1 << 22) + 3, 0, 0, 123), (1_249_283, 0, 0, (1 << 32) - 600_001)])
 def test_stochastic_round_fp16_bit_exact(n, pad_in, pad_out, goff):
     """fp32 -> fp16 stochastic rounding, bit-exact against the oracle: fp16
     subnormals, the subnormal/normal boundary, 65504 .. 65536 and beyond,
@@ -168,13 +219,13 @@ def test_stochastic_round_fp16_bit_exact(n, pad_in, pad_out, goff):
     assert_bit_equal(got, oracle.stochastic_round_fp16(x, goff, seed), "sr fp16")
 
 
+@pytest.mark.parametrize("n", [2048 * 300 + 777, 2048 * 700 + 777])
 @pytest.mark.parametrize("goff", [0, (1 << 32) - 3001])
-def test_stochastic_round_fp16_weights_and_scattered_specials(goff):
+def test_stochastic_round_fp16_weights_and_scattered_specials(goff, n):
     """Weight-like values (N(0, 0.02), all in fp16's normal range) over many
     tiles and a ragged tail, then the same with one zero, subnormal, NaN or
     overflow scattered into some warps' elements: every warp shape of the
     vector kernel (all normal, some special) is bit-exact against the oracle."""
-    n = 2048 * 300 + 777
     rng = np.random.default_rng(11)
     x = (rng.standard_normal(n) * 0.02).astype(np.float32)
     x = np.where(np.abs(x) < 2.0 ** -13, np.float32(0.5), x).astype(np.float32)
