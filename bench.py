@@ -703,6 +703,23 @@ def measure_sr_stress(mp, stream, device, peak, n=64 << 20, steps=1000):
                                         "gbs": round(SR_BYTES * n / ms / 1e6, 1),
                                         "frac": round(SR_BYTES * n / ms / 1e6 / peak, 4),
                                         "bytes_per_elem": SR_BYTES}}
+    # the same launches back to back between one pair of events: each launch's
+    # start overlaps the previous one's end (programmatic dependent launch),
+    # so the per-launch latency that the figure above includes drops out; the
+    # 403 MB per launch stay above the 129 MB L2, and every launch starts at
+    # the front of the arrays, which the previous one left long ago
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    chained = 20
+    a.record(stream)
+    for _ in range(chained):
+        mp.mp_stochastic_round(out16, w0, 7, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cms = a.elapsed_time(b) / chained
+    res["sr_kernel_chained"] = {"ms": round(cms, 5), "launches": chained, "gelems_s": round(n / cms / 1e6, 2),
+                                "gbs": round(SR_BYTES * n / cms / 1e6, 1),
+                                "frac": round(SR_BYTES * n / cms / 1e6 / peak, 4),
+                                "what": "mean over back-to-back launches between one pair of CUDA events"}
     delta = (w0.abs() * 1e-4).float()
     fp32 = w0.clone()
     sr = w0.to(torch.bfloat16)
