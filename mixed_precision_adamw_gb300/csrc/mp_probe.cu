@@ -25,6 +25,8 @@
 
 #include <cuda_runtime.h>
 
+#include "mp_tma.cuh"
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -69,7 +71,6 @@ copy_probe(uint4* __restrict__ dst, const uint4* __restrict__ src, uint64_t n) {
 // ---- TMA bulk-copy probes ---------------------------------------------------
 constexpr int kBulkMaxStreams = 4;
 constexpr int kBulkMaxStages = 8;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 
 struct BulkStreams {
   const uint8_t* load[kBulkMaxStreams];  // tile t of stream i starts at load[i] + t * load_bytes[i]
@@ -81,34 +82,8 @@ struct BulkStreams {
   uint32_t stage_bytes;  // sum of load_bytes, a multiple of 128
   int32_t stages;        // 2 .. kBulkMaxStages
   int32_t hint;          // 1: L2 evict-first policy on every copy
+  uint32_t extra_tx;     // bytes a stage's barrier expects beyond its loads (0; > 0 only to test give-up)
 };
-
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Waits for the phase of `bar` with the given parity to complete, for at
-// most kWaitLimitNs; false if it gave up.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = now_ns();
-  while (!bar_try_wait(bar, parity))
-    if (now_ns() - t0 > kWaitLimitNs) return false;
-  return true;
-}
 
 __global__ void __launch_bounds__(32)
 bulk_streams_probe(const __grid_constant__ BulkStreams s, uint64_t ntiles, uint32_t* __restrict__ err) {
@@ -117,18 +92,16 @@ bulk_streams_probe(const __grid_constant__ BulkStreams s, uint64_t ntiles, uint3
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   const uint32_t bars = base + static_cast<uint32_t>(s.stages) * s.stage_bytes;
   const uint32_t S = static_cast<uint32_t>(s.stages);
-  for (uint32_t i = 0; i < S; ++i) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8 * i) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  uint64_t policy = 0;
-  if (s.hint) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  for (uint32_t i = 0; i < S; ++i) mpk::mbar_init(bars + 8 * i, 1);
+  mpk::mbar_init_fence();
+  const uint64_t policy = s.hint ? mpk::l2_evict_first() : 0;
 
   const uint64_t first = blockIdx.x, step = gridDim.x;
   const uint64_t mine = first < ntiles ? (ntiles - 1 - first) / step + 1 : 0;  // this block's tiles
   auto issue_load = [&](uint64_t k) {
     const uint32_t st = static_cast<uint32_t>(k % S), bar = bars + 8 * st;
     const uint64_t tile = first + k * step;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(s.stage_bytes) : "memory");
+    mpk::mbar_expect_tx(bar, s.stage_bytes + s.extra_tx);
     uint32_t off = base + st * s.stage_bytes;
     for (int i = 0; i < s.nload; ++i) {
       const uint8_t* src = s.load[i] + tile * s.load_bytes[i];
@@ -148,7 +121,7 @@ bulk_streams_probe(const __grid_constant__ BulkStreams s, uint64_t ntiles, uint3
   bool ok = true;
   for (; k < mine; ++k) {
     const uint32_t st = static_cast<uint32_t>(k % S);
-    if (!bar_wait(bars + 8 * st, static_cast<uint32_t>((k / S) & 1))) {
+    if (!mpk::mbar_wait(bars + 8 * st, static_cast<uint32_t>((k / S) & 1))) {
       ok = false;
       break;
     }
@@ -174,7 +147,7 @@ bulk_streams_probe(const __grid_constant__ BulkStreams s, uint64_t ntiles, uint3
   if (!ok) {
     atomicExch(err, 1u);
     for (uint64_t j = k; j < issued; ++j)  // loads still in flight: bounded waits
-      bar_wait(bars + 8 * static_cast<uint32_t>(j % S), static_cast<uint32_t>((j / S) & 1));
+      mpk::mbar_wait(bars + 8 * static_cast<uint32_t>(j % S), static_cast<uint32_t>((j / S) & 1));
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -284,6 +257,26 @@ int mp_probe_copy_bulk(void* dst, const void* src, uint64_t tiles, int blocks_pe
   s.stages = stages;
   s.hint = hint ? 1 : 0;
   return launch_bulk(s, tiles, blocks_per_sm, d_err, static_cast<cudaStream_t>(stream));
+}
+
+// The bulk copy probe over `tiles` 28,672-byte tiles of `buf` (dst = the
+// second half) with every stage's mbarrier told to expect 16 bytes more than
+// its loads bring: every load lands, but no stage's phase completes, so each
+// block's bounded waits give up (one second each, for the wait and for the
+// one load in flight) and set *d_err. For testing that give-up path; nothing
+// faults or hangs. buf: device, 16-B aligned, 2 * tiles * 28,672 bytes.
+int mp_probe_bulk_timeout(void* buf, uint64_t tiles, uint32_t* d_err, void* stream) {
+  if (buf == nullptr || !aligned16(buf) || tiles == 0) return static_cast<int>(cudaErrorInvalidValue);
+  BulkStreams s{};
+  s.nload = 1;
+  s.load[0] = static_cast<const uint8_t*>(buf);
+  s.load_bytes[0] = s.stage_bytes = kTile * 14;
+  s.nstore = 1;
+  s.store[0] = static_cast<uint8_t*>(buf) + tiles * (kTile * 14);
+  s.store_bytes[0] = kTile * 14;
+  s.stages = 2;
+  s.extra_tx = 16;
+  return launch_bulk(s, tiles, 1, d_err, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -5,6 +5,7 @@ the gradient's bits, through register loads and through TMA bulk copies;
 the bulk copy probe copies its tiles exactly. No probe wait may give up."""
 import ctypes
 import os
+import time
 
 import pytest
 import torch
@@ -26,6 +27,7 @@ def probe():
     lib.mp_probe_step_streams.argtypes = [vp, vp, vp, vp, vp, u64, i32, vp]
     lib.mp_probe_step_streams_bulk.argtypes = [vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp]
     lib.mp_probe_copy_bulk.argtypes = [vp, vp, u64, i32, i32, i32, vp, vp]
+    lib.mp_probe_bulk_timeout.argtypes = [vp, u64, vp, vp]
     return lib
 
 
@@ -90,3 +92,24 @@ def test_bulk_probe_refuses_bad_arguments(probe):
                                             s) != 0  # unaligned
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+def test_bounded_mbarrier_wait_gives_up_and_reports(probe):
+    """The staged kernels' mbarrier waits give up after one second of the
+    global timer instead of spinning forever. Here every stage's barrier is
+    told to expect 16 bytes more than its bulk load brings, so no phase ever
+    completes (every byte lands; nothing faults): the kernel must end on its
+    own within a few seconds, report the give-up in its error word, and leave
+    the GPU usable (a normal probe afterwards moves its bytes exactly)."""
+    tiles = torch.cuda.get_device_properties(0).multi_processor_count
+    buf = torch.zeros(2 * tiles * TILE * 14, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    rc = probe.mp_probe_bulk_timeout(buf.data_ptr(), tiles, err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert int(err.item()) == 1
+    assert 0.9 < elapsed < 30, elapsed  # one-second waits, not an endless spin
+    test_bulk_copy_probe_copies_its_tiles(probe, 1, 7, 1)
