@@ -1,13 +1,16 @@
-// mp_step.cu — the fused AdamW + stochastic-rounding step kernel.
+// mp_step.cu — the fused AdamW + stochastic-rounding step kernels.
 //
 // llm.c walk-through ch. 04 "Multi-GPU and mixed precision" §2.2: one pass
 // per parameter reads the bf16 gradient and the fp32 master/m/v, writes the
-// fp32 master/m/v and the stochastically rounded bf16 weight. The kernel is
-// bound by HBM traffic (28 B per parameter with master, 22 B without), so it
-// is written as coalesced 16-B (fp32) and 8-B (bf16) vector streams over all
-// arrays in one pass, in a grid-stride loop of persistent blocks sized to the
-// SM count. Weight decay comes from a per-launch table of decay segments
-// (maximal runs of tensors with equal decay flag, §2.2's "2D tensors only").
+// fp32 master/m/v and the stochastically rounded bf16 weight. The step is
+// bound by HBM traffic (28 B per parameter with master, 22 B without). Long
+// ranges run adamw_tma_kernel, which stages whole tiles of every stream
+// through shared memory with the TMA engine's bulk copies while its warps
+// compute; other ranges run the register kernels, coalesced 16-B (fp32) and
+// 8-B (bf16) vector streams in a grid-stride loop of persistent blocks sized
+// to the SM count. All give the same bits. Weight decay comes from a
+// per-launch table of decay segments (maximal runs of tensors with equal
+// decay flag, §2.2's "2D tensors only").
 #include <atomic>
 #include <cmath>
 
@@ -19,7 +22,7 @@
 namespace mpk {
 namespace {
 
-// Resident blocks per SM the vector kernel is compiled for: the with-master
+// Resident blocks per SM the register vector kernel is compiled for: the with-master
 // kernel keeps 3 blocks of 256 threads (it compiles to 72 registers; forcing 4
 // blocks, i.e. at most 64 registers, was 8 % slower on GB300); the no-master
 // kernel moves fewer bytes per element and runs 9 % faster at 4 blocks (63
