@@ -46,14 +46,16 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
 // Level 1 with the gradients staged through shared memory by the TMA engine,
 // for 16-B aligned device gradients: the element mapping and the order of
 // every addition are norm_partial_kernel's, so each partial has the same bits.
-// Block b's vectors of iteration j, b*256 + j*nblocks*256 + t for t < 256,
-// are one contiguous 4 KB piece. Thread 0 has groups of kNormPiecesPerStage
-// pieces loaded by bulk copies into a ring of kNormTmaStages stages while the
-// block adds the pieces of an earlier group in order (thread t the vector t
-// of each); a stage is loaded again once every warp has read it (an mbarrier
-// per stage each way). Measured on GB300 (Llama-3-8B gradients, 16 GB): 4
-// pieces x 3 stages 2.46 ms; 3 x 4 2.50; 6 x 2 2.65; 2 x 6 3.09; 1 x 8 2.90;
-// the register kernel 2.55 ms in the same shared-memory configuration. The
+// Launched only where norm_map gives each block a contiguous run of 256-vector
+// (4 KB) pieces. Thread 0 has groups of kNormPiecesPerStage consecutive pieces
+// loaded, one bulk copy per group, into a ring of kNormTmaStages stages while
+// the block adds the pieces of an earlier group in order (thread t the vector
+// t of each); a stage is loaded again once every warp has read it (an
+// mbarrier per stage each way). Measured on GB300 (Llama-3-8B gradients,
+// 16 GB): 4 pieces x 3 stages 2.15 ms; 8 x 2 3.03. With the blocks'
+// pieces interleaved (4 KB bulk copies, 1 to 8 per group) the best shape took
+// 2.46 ms (4 x 3; 3 x 4 2.50; 6 x 2 2.65; 2 x 6 3.09; 1 x 8 2.90), and the
+// register kernel 2.55 ms in the same shared-memory configuration. The
 // loads do not pass through L1, so the kernel keeps its rate with most of the
 // SM's memory as shared memory, where the TMA-staged step kernel must run
 // beside or after it (with it the norm -> update boundary of a step costs
@@ -74,10 +76,11 @@ norm_partial_tma_kernel(const uint16_t* __restrict__ grads, uint64_t n, double* 
   pdl_enter();
   constexpr uint32_t S = kNormTmaStages, G = kNormPiecesPerStage;
   const uint32_t base = smem_u32(ring), full = base + S * kNormStageBytes, done = full + 8 * S;
-  const uint64_t nvec = n / 8, stride = static_cast<uint64_t>(gridDim.x) * kThreads;
-  const uint64_t first = static_cast<uint64_t>(blockIdx.x) * kThreads;  // vector 0 of piece 0
-  const uint64_t pieces = first < nvec ? (nvec - first - 1) / stride + 1 : 0;
-  const uint64_t groups = (pieces + G - 1) / G;  // stage loads: pieces G*q .. G*q + G - 1
+  const uint64_t nvec = n / 8;
+  const NormMap map = norm_map(nvec, blockIdx.x, gridDim.x);  // contiguous: the launch ensures it
+  const uint64_t first = map.first, last = map.last;
+  const uint64_t pieces = (last - first + kThreads - 1) / kThreads;  // 256-vector pieces
+  const uint64_t groups = (pieces + G - 1) / G;  // one bulk copy: pieces G*q .. G*q + G - 1
   if (threadIdx.x == 0) {
     gave_up = 0;
     for (uint32_t i = 0; i < S; ++i) {
@@ -91,18 +94,11 @@ norm_partial_tma_kernel(const uint16_t* __restrict__ grads, uint64_t n, double* 
   uint64_t policy = 0, issued = 0;
   auto load = [&](uint64_t q) {
     const uint32_t st = static_cast<uint32_t>(q % S);
-    const uint64_t p1 = (q + 1) * G < pieces ? (q + 1) * G : pieces;
-    uint32_t total = 0;
-    for (uint64_t p = q * G; p < p1; ++p) {
-      const uint64_t left = nvec - (first + p * stride);
-      total += static_cast<uint32_t>((left < kThreads ? left : kThreads) * 16);
-    }
-    mbar_expect_tx(full + 8 * st, total);
-    for (uint64_t p = q * G; p < p1; ++p) {
-      const uint64_t v0 = first + p * stride, left = nvec - v0;
-      bulk_load(base + st * kNormStageBytes + static_cast<uint32_t>(p - q * G) * kNormPieceBytes, g4 + v0,
-                static_cast<uint32_t>((left < kThreads ? left : kThreads) * 16), full + 8 * st, policy);
-    }
+    const uint64_t v0 = first + q * G * kThreads;
+    const uint64_t v1 = v0 + G * kThreads < last ? v0 + G * kThreads : last;
+    const uint32_t bytes = static_cast<uint32_t>((v1 - v0) * 16);
+    mbar_expect_tx(full + 8 * st, bytes);
+    bulk_load(base + st * kNormStageBytes, g4 + v0, bytes, full + 8 * st, policy);
   };
   bool producing = threadIdx.x == 0;
   if (producing) {
@@ -121,7 +117,7 @@ norm_partial_tma_kernel(const uint16_t* __restrict__ grads, uint64_t n, double* 
 #pragma unroll
     for (uint32_t g = 0; g < G; ++g) {
       const uint64_t p = q * G + g;
-      if (p < pieces && first + p * stride + threadIdx.x < nvec)
+      if (p < pieces && first + p * kThreads + threadIdx.x < last)
         acc(s, c, sumsq8(*reinterpret_cast<const uint4*>(sp + g * kNormPieceBytes)));
     }
     __syncwarp();

@@ -68,20 +68,46 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
   return r;
 }
 
-// Partial sum of squares of norm block `block` out of `nblocks` (the element
-// mapping of a grid of nblocks blocks): thread t of the block takes the
-// 8-element vectors block*256 + t + j*nblocks*256 and the scalar tail alike.
-// vec: grads (and copy_out) 16-B aligned, processed as 8-element vectors
-// plus a scalar tail. kCopy: grads may live in page-locked host memory (read
-// over the host link) and every element read is also written to copy_out, so
-// the host-to-device transfer and the norm are one pass; the arithmetic and
-// its order are the same as without the copy. Every thread of the block
-// calls it and receives the block's partial.
+// Which 8-element vectors norm block `block` of `nblocks` adds, and in what
+// order. Long ranges (at least two 256-vector pieces per block) give each
+// block one contiguous run of whole 256-vector pieces, `per` vectors long
+// (ceil(nvec / nblocks) rounded up to 256; the last blocks' runs end early or
+// are empty): thread t takes vector t of each piece, in piece order, so a
+// block's loads are long contiguous spans (the TMA-staged kernel fetches a
+// group of pieces with one bulk copy). Shorter ranges interleave the blocks:
+// thread t of block b takes vectors b*256 + t + j*nblocks*256. Every kernel
+// of the norm uses this, so the host- and device-gradient kernels add the
+// same squares in the same order.
+struct NormMap {
+  bool contiguous;
+  uint64_t first, last;  // contiguous: this block's vectors [first, last)
+};
+
+__device__ __forceinline__ NormMap norm_map(uint64_t nvec, uint32_t block, uint32_t nblocks) {
+  NormMap m{false, 0, 0};
+  const uint64_t stride = static_cast<uint64_t>(nblocks) * kThreads;
+  if (nvec < 2 * stride) return m;
+  m.contiguous = true;
+  const uint64_t per = ((nvec + nblocks - 1) / nblocks + kThreads - 1) / kThreads * kThreads;
+  m.first = static_cast<uint64_t>(block) * per < nvec ? static_cast<uint64_t>(block) * per : nvec;
+  m.last = m.first + per < nvec ? m.first + per : nvec;
+  return m;
+}
+
 template <bool kCopy>
 __device__ __forceinline__ double norm_block_finish(const uint16_t* __restrict__ grads, uint64_t n, int vec,
                                                     uint16_t* __restrict__ copy_out, uint32_t block,
                                                     uint32_t nblocks, double* sh, float s, float c);
 
+// Partial sum of squares of norm block `block` out of `nblocks`: its vectors
+// as norm_map assigns them, then its share of the scalar tail (thread t of
+// block b takes elements nvec*8 + b*256 + t + j*nblocks*256). vec: grads (and
+// copy_out) 16-B aligned, processed as 8-element vectors plus a scalar tail.
+// kCopy: grads may live in page-locked host memory (read over the host link)
+// and every element read is also written to copy_out, so the host-to-device
+// transfer and the norm are one pass; the arithmetic and its order are the
+// same as without the copy. Every thread of the block calls it and receives
+// the block's partial.
 template <bool kCopy>
 __device__ __forceinline__ double norm_block_partial(const uint16_t* __restrict__ grads, uint64_t n, int vec,
                                                      uint16_t* __restrict__ copy_out, uint32_t block,
@@ -93,6 +119,28 @@ __device__ __forceinline__ double norm_block_partial(const uint16_t* __restrict_
   const uint64_t k0 = static_cast<uint64_t>(block) * kThreads + threadIdx.x;
 
   float s = 0.0f, c = 0.0f;
+  const NormMap map = norm_map(nvec, block, nblocks);
+  if (map.contiguous) {
+    uint64_t k = map.first + threadIdx.x;
+    constexpr uint64_t kStep = kThreads;
+    for (; k + (kNormUnroll - 1) * kStep < map.last; k += kNormUnroll * kStep) {
+      uint4 w[kNormUnroll];
+#pragma unroll
+      for (int u = 0; u < kNormUnroll; ++u) w[u] = __ldcs(g4 + k + u * kStep);
+      if (kCopy) {
+#pragma unroll
+        for (int u = 0; u < kNormUnroll; ++u) c4[k + u * kStep] = w[u];
+      }
+#pragma unroll
+      for (int u = 0; u < kNormUnroll; ++u) acc(s, c, sumsq8(w[u]));
+    }
+    for (; k < map.last; k += kStep) {
+      const uint4 w = __ldcs(g4 + k);
+      if (kCopy) c4[k] = w;
+      acc(s, c, sumsq8(w));
+    }
+    return norm_block_finish<kCopy>(grads, n, vec, copy_out, block, nblocks, sh, s, c);
+  }
   uint64_t k = k0;
   for (; k + (kNormUnroll - 1) * stride < nvec; k += kNormUnroll * stride) {
     uint4 w[kNormUnroll];
@@ -139,7 +187,12 @@ __device__ __forceinline__ double norm_block_finish(const uint16_t* __restrict__
     const uint4* r4 = kCopy ? reinterpret_cast<const uint4*>(copy_out) : g4;
     const uint16_t* r1 = kCopy ? copy_out : grads;
     double d = 0.0;
-    for (k = k0; k < nvec; k += stride) d = __dadd_rn(d, dsumsq8(r4[k]));
+    const NormMap map = norm_map(nvec, block, nblocks);
+    if (map.contiguous) {
+      for (k = map.first + threadIdx.x; k < map.last; k += kThreads) d = __dadd_rn(d, dsumsq8(r4[k]));
+    } else {
+      for (k = k0; k < nvec; k += stride) d = __dadd_rn(d, dsumsq8(r4[k]));
+    }
     for (uint64_t i = nvec * 8 + k0; i < n; i += stride) {
       const double x = bf16_to_f32(r1[i]);
       d = __dadd_rn(d, __dmul_rn(x, x));
