@@ -119,9 +119,10 @@ int mp_last_cuda_error(void);
  *   d_scale     float[1], device, written (feeds mp_adamw_step).
  *   d_sumsq     double[1], device, written; may be NULL.
  * Launches: 16-B aligned gradients of at least 16,384 elements per SM have
- * the first level stage its reads through shared memory with the TMA engine
- * (49 KB per block); it adds the same squares in the same order as the
- * register kernel used otherwise, so the result is the same bits. If one of
+ * each first-level block read one contiguous run of them, staged through
+ * shared memory by the TMA engine (49 KB per block); it adds the same squares
+ * in the same order as the register kernel that reads host gradients
+ * (mp_optimizer_step's host_grads), so the result is the same bits. If one of
  * its bounded waits gives up (only a fault of the GPU or of the library can
  * cause that), the norm and the scale come out NaN.
  * Errors: MP_ERR_NULL, MP_ERR_ALIGN, MP_ERR_RANGE (clip), MP_ERR_WORKSPACE,

@@ -46,22 +46,23 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
 // Level 1 with the gradients staged through shared memory by the TMA engine,
 // for 16-B aligned device gradients: the element mapping and the order of
 // every addition are norm_partial_kernel's, so each partial has the same bits.
-// Launched only where norm_map gives each block a contiguous run of 256-vector
-// (4 KB) pieces. Thread 0 has groups of kNormPiecesPerStage consecutive pieces
-// loaded, one bulk copy per group, into a ring of kNormTmaStages stages while
-// the block adds the pieces of an earlier group in order (thread t the vector
-// t of each); a stage is loaded again once every warp has read it (an
-// mbarrier per stage each way). Measured on GB300 (Llama-3-8B gradients,
-// 16 GB): 4 pieces x 3 stages 2.15 ms; 8 x 2 3.03. With the blocks'
-// pieces interleaved (4 KB bulk copies, 1 to 8 per group) the best shape took
-// 2.46 ms (4 x 3; 3 x 4 2.50; 6 x 2 2.65; 2 x 6 3.09; 1 x 8 2.90), and the
-// register kernel 2.55 ms in the same shared-memory configuration. The
-// loads do not pass through L1, so the kernel keeps its rate with most of the
-// SM's memory as shared memory, where the TMA-staged step kernel must run
-// beside or after it (with it the norm -> update boundary of a step costs
-// nothing measurable; with the register kernel it cost 0.3 ms). Every wait
-// gives up after one second; a block that gave up writes a NaN partial, so
-// the norm and scale come out NaN and the step refuses to run.
+// Launched only where norm_map gives each block a contiguous run of 4 KB
+// pieces (256 vectors; its last piece shorter). Thread 0 has groups of
+// kNormPiecesPerStage consecutive pieces loaded, one bulk copy per group,
+// into a ring of kNormTmaStages stages while the block adds the pieces of an
+// earlier group in order (thread t the vector t of each); a stage is loaded
+// again once every warp has read it (an mbarrier per stage each way).
+// Measured on GB300 (Llama-3-8B gradients, 16 GB): 4 pieces x 3 stages
+// 2.15-2.18 ms; 8 x 2 3.03. With the blocks' pieces interleaved (4 KB bulk
+// copies, 1 to 8 per group) the best shape took 2.46 ms (4 x 3; 3 x 4 2.50;
+// 6 x 2 2.65; 2 x 6 3.09; 1 x 8 2.90), and the register kernel 2.55 ms in
+// the same shared-memory configuration. The loads do not pass through L1, so
+// the kernel keeps its rate with most of the SM's memory as shared memory,
+// where the TMA-staged step kernel must run beside or after it (with it the
+// norm -> update boundary of a step costs nothing measurable; with the
+// register kernel it cost 0.3 ms). Every wait gives up after one second; a
+// block that gave up writes a NaN partial, so the norm and scale come out NaN
+// and the step refuses to run.
 constexpr uint32_t kNormTmaStages = 3;
 constexpr uint32_t kNormPiecesPerStage = 4;
 constexpr uint32_t kNormPieceBytes = kThreads * 16;
