@@ -47,11 +47,11 @@ norm_partial_kernel(const uint16_t* __restrict__ grads, uint64_t n, int vec, dou
 // for 16-B aligned device gradients: the element mapping and the order of
 // every addition are norm_partial_kernel's, so each partial has the same bits.
 // Launched only where norm_map gives each block a contiguous run of 4 KB
-// pieces (256 vectors; its last piece shorter). Thread 0 has groups of
-// kNormPiecesPerStage consecutive pieces loaded, one bulk copy per group,
-// into a ring of kNormTmaStages stages while the block adds the pieces of an
-// earlier group in order (thread t the vector t of each); a stage is loaded
-// again once every warp has read it (an mbarrier per stage each way).
+// pieces (256 vectors each). Thread 0 has groups of kNormPiecesPerStage
+// consecutive pieces loaded, one bulk copy per group, into a ring of
+// kNormTmaStages stages while the block adds the pieces of an earlier group
+// in order (thread t the vector t of each); a stage is loaded again once
+// every warp has read it (an mbarrier per stage each way).
 // Measured on GB300 (Llama-3-8B gradients, 16 GB): 4 pieces x 3 stages
 // 2.15-2.18 ms; 8 x 2 3.03. With the blocks' pieces interleaved (4 KB bulk
 // copies, 1 to 8 per group) the best shape took 2.46 ms (4 x 3; 3 x 4 2.50;

@@ -71,10 +71,13 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
 // Which 8-element vectors norm block `block` of `nblocks` adds, and in what
 // order. Long ranges (at least two 256-vector pieces per block) give each
 // block one contiguous run of `per` vectors (ceil(nvec / nblocks) rounded up
-// to 8, whole 128-B lines; the last block's run ends early), cut into pieces
-// of 256 vectors from its start (the last one shorter): thread t takes vector
-// t of each piece, in piece order, so a block's loads are long contiguous
-// spans (the TMA-staged kernel fetches a group of pieces with one bulk copy).
+// to whole 256-vector pieces, so every run starts on a 4 KB boundary of the
+// buffer; the last runs end early or are empty): thread t takes vector t of
+// each piece, in piece order, so a block's loads are long contiguous spans
+// (the TMA-staged kernel fetches a group of pieces with one bulk copy).
+// Measured on GB300 (Llama-3-8B gradients): the staged norm took 2.174-2.176
+// ms with runs of whole pieces and 2.203-2.206 ms with runs rounded only to
+// 128-B lines (better balanced, the same chained step time).
 // Shorter ranges interleave the blocks:
 // thread t of block b takes vectors b*256 + t + j*nblocks*256. Every kernel
 // of the norm uses this, so the host- and device-gradient kernels add the
@@ -89,7 +92,7 @@ __device__ __forceinline__ NormMap norm_map(uint64_t nvec, uint32_t block, uint3
   const uint64_t stride = static_cast<uint64_t>(nblocks) * kThreads;
   if (nvec < 2 * stride) return m;
   m.contiguous = true;
-  const uint64_t per = ((nvec + nblocks - 1) / nblocks + 7) / 8 * 8;  // whole 128-B lines
+  const uint64_t per = ((nvec + nblocks - 1) / nblocks + kThreads - 1) / kThreads * kThreads;
   m.first = static_cast<uint64_t>(block) * per < nvec ? static_cast<uint64_t>(block) * per : nvec;
   m.last = m.first + per < nvec ? m.first + per : nvec;
   return m;
