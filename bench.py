@@ -583,6 +583,7 @@ def measure_stream_probes(st, g, N, stream, peak):
     lib.mp_probe_step_streams.argtypes = [vp, vp, vp, vp, vp, u64, i32, vp]
     lib.mp_probe_copy.argtypes = [vp, vp, u64, i32, vp]
     lib.mp_probe_step_streams_bulk.argtypes = [vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp]
+    lib.mp_probe_step_streams_bulk_tile.argtypes = [vp, vp, vp, vp, vp, u64, ctypes.c_uint32, i32, i32, i32, vp, vp]
     lib.mp_probe_copy_bulk.argtypes = [vp, vp, u64, i32, i32, i32, vp, vp]
     err = torch.zeros(1, dtype=torch.int32, device=g.device)
     chunk = 201_326_592  # the step's launch size on the large sets (whole 2048-element tiles)
@@ -614,6 +615,23 @@ def measure_stream_probes(st, g, N, stream, peak):
         key = f"step_streams_tma_bulk_{bps}_blocks_per_sm_{stages}_stages" + ("_evict_first" if hint else "")
         out[key] = {"gbs": round(STEP_BYTES_MASTER * n / ms / 1e6, 1),
                     "frac": round(STEP_BYTES_MASTER * n / ms / 1e6 / peak, 4), "ms": round(ms, 5)}
+    # larger tiles with one tile of loads in flight per SM (launches stay multiples of the tile)
+    for tile in (6144, 8192):
+        nt = N // tile * tile
+        if nt == 0:
+            continue
+        def run_bulk_tile():
+            for a in range(0, nt, chunk):
+                b = min(nt, a + chunk)
+                rc = lib.mp_probe_step_streams_bulk_tile(st["params"][a:].data_ptr(), g[a:].data_ptr(),
+                                                         st["master"][a:].data_ptr(), st["m"][a:].data_ptr(),
+                                                         st["v"][a:].data_ptr(), b - a, tile, 1, 2, 1,
+                                                         err.data_ptr(), stream.cuda_stream)
+                assert rc == 0, rc
+        ms = time_events(run_bulk_tile, 5, stream)
+        out[f"step_streams_tma_bulk_{tile}_tiles_1_blocks_per_sm_2_stages_evict_first"] = {
+            "gbs": round(STEP_BYTES_MASTER * nt / ms / 1e6, 1),
+            "frac": round(STEP_BYTES_MASTER * nt / ms / 1e6 / peak, 4), "ms": round(ms, 5)}
     nbytes = min(STEP_BYTES_MASTER // 2 * N, 1 << 32) // 16 * 16
     src = torch.empty(nbytes, dtype=torch.uint8, device=g.device)
     dst = torch.empty_like(src)
@@ -640,7 +658,8 @@ def measure_stream_probes(st, g, N, stream, peak):
     del src, dst
     out["what"] = ("compute-free SM kernels: the step's streams (28 B/param, written back unchanged) in "
                    f"launches of {chunk} params, through registers and through TMA bulk copies staged in "
-                   f"shared memory (one issuing thread per block, 28 KB stages); a 16-B copy of {nbytes} bytes "
+                   f"shared memory (one issuing thread per block, stages of 2048-param tiles (28 KB) or of "
+                   f"6144 and 8192 params); a 16-B copy of {nbytes} bytes "
                    "and a TMA bulk copy of its whole 28 KB tiles")
     return out
 

@@ -15,8 +15,9 @@
 //
 // The third and fourth probes move the same streams through shared memory
 // with the TMA engine's 1D bulk copies instead of register loads: one thread
-// per block issues, per 2048-element tile, four bulk loads (gradient,
-// master, m, v: 28 KB) that complete on a stage's mbarrier, then four bulk
+// per block issues, per tile (2048 elements: 28 KB, or a given multiple of
+// 64), four bulk loads (gradient, master, m, v) that complete on a stage's
+// mbarrier, then four bulk
 // stores from the staged tile (master, m and v back, the gradient's bits into
 // the weight), with several stages in flight per block; and a plain bulk
 // copy in 28 KB tiles. Every wait on an mbarrier gives up after one second
@@ -206,15 +207,18 @@ int mp_probe_copy(void* dst, const void* src, uint64_t n_vec16, int blocks_per_s
   return static_cast<int>(cudaGetLastError());
 }
 
-// The step's streams over n parameters (n a multiple of 2048; every pointer
-// 16-B aligned) through TMA bulk copies: blocks_per_sm blocks of one issuing
-// thread per SM, `stages` 28 KB stages each (2 .. 8, and they must fit in
-// shared memory), hint 1 for an L2 evict-first policy. *d_err (device) is set
-// to 1 if a wait gave up. Returns a cudaError_t.
-int mp_probe_step_streams_bulk(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
-                               uint64_t n, int blocks_per_sm, int stages, int hint, uint32_t* d_err, void* stream) {
-  if (n % kTile || !aligned16(params) || !aligned16(grads) || !aligned16(master) || !aligned16(m) ||
-      !aligned16(v))
+// The step's streams over n parameters through TMA bulk copies, in tiles of
+// `tile` parameters (a multiple of 64, so that a stage of tile * 14 bytes
+// keeps the next one 128-B aligned; n a multiple of tile; every pointer 16-B
+// aligned): blocks_per_sm blocks of one issuing thread per SM, `stages`
+// stages each (2 .. 8, and they must fit in shared memory), hint 1 for an L2
+// evict-first policy. *d_err (device) is set to 1 if a wait gave up. Returns
+// a cudaError_t.
+int mp_probe_step_streams_bulk_tile(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
+                                    uint64_t n, uint32_t tile, int blocks_per_sm, int stages, int hint,
+                                    uint32_t* d_err, void* stream) {
+  if (tile == 0 || tile % 64 || tile > (1u << 20) || n % tile || !aligned16(params) || !aligned16(grads) ||
+      !aligned16(master) || !aligned16(m) || !aligned16(v))
     return static_cast<int>(cudaErrorInvalidValue);
   BulkStreams s{};
   s.nload = 4;
@@ -222,23 +226,30 @@ int mp_probe_step_streams_bulk(uint16_t* params, const uint16_t* grads, float* m
   s.load[1] = reinterpret_cast<const uint8_t*>(master);
   s.load[2] = reinterpret_cast<const uint8_t*>(m);
   s.load[3] = reinterpret_cast<const uint8_t*>(v);
-  s.load_bytes[0] = kTile * 2;
-  s.load_bytes[1] = s.load_bytes[2] = s.load_bytes[3] = kTile * 4;
-  s.stage_bytes = kTile * 14;  // 28,672 B
+  s.load_bytes[0] = tile * 2;
+  s.load_bytes[1] = s.load_bytes[2] = s.load_bytes[3] = tile * 4;
+  s.stage_bytes = tile * 14;
   s.nstore = 4;
   s.store[0] = reinterpret_cast<uint8_t*>(master);
   s.store[1] = reinterpret_cast<uint8_t*>(m);
   s.store[2] = reinterpret_cast<uint8_t*>(v);
   s.store[3] = reinterpret_cast<uint8_t*>(params);
-  s.store_bytes[0] = s.store_bytes[1] = s.store_bytes[2] = kTile * 4;
-  s.store_bytes[3] = kTile * 2;
-  s.store_from[0] = kTile * 2;   // master's staged tile
-  s.store_from[1] = kTile * 6;   // m's
-  s.store_from[2] = kTile * 10;  // v's
-  s.store_from[3] = 0;           // the gradient's bits into the weight
+  s.store_bytes[0] = s.store_bytes[1] = s.store_bytes[2] = tile * 4;
+  s.store_bytes[3] = tile * 2;
+  s.store_from[0] = tile * 2;   // master's staged tile
+  s.store_from[1] = tile * 6;   // m's
+  s.store_from[2] = tile * 10;  // v's
+  s.store_from[3] = 0;          // the gradient's bits into the weight
   s.stages = stages;
   s.hint = hint ? 1 : 0;
-  return launch_bulk(s, n / kTile, blocks_per_sm, d_err, static_cast<cudaStream_t>(stream));
+  return launch_bulk(s, n / tile, blocks_per_sm, d_err, static_cast<cudaStream_t>(stream));
+}
+
+// mp_probe_step_streams_bulk_tile with 2048-parameter (28 KB) tiles.
+int mp_probe_step_streams_bulk(uint16_t* params, const uint16_t* grads, float* master, float* m, float* v,
+                               uint64_t n, int blocks_per_sm, int stages, int hint, uint32_t* d_err, void* stream) {
+  return mp_probe_step_streams_bulk_tile(params, grads, master, m, v, n, kTile, blocks_per_sm, stages, hint, d_err,
+                                         stream);
 }
 
 // dst <- src in `tiles` tiles of 28,672 B through TMA bulk copies (both

@@ -26,6 +26,7 @@ def probe():
     vp, u64, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int
     lib.mp_probe_step_streams.argtypes = [vp, vp, vp, vp, vp, u64, i32, vp]
     lib.mp_probe_step_streams_bulk.argtypes = [vp, vp, vp, vp, vp, u64, i32, i32, i32, vp, vp]
+    lib.mp_probe_step_streams_bulk_tile.argtypes = [vp, vp, vp, vp, vp, u64, ctypes.c_uint32, i32, i32, i32, vp, vp]
     lib.mp_probe_copy_bulk.argtypes = [vp, vp, u64, i32, i32, i32, vp, vp]
     lib.mp_probe_bulk_timeout.argtypes = [vp, u64, vp, vp]
     return lib
@@ -62,6 +63,24 @@ def test_step_stream_probes_move_the_step_bytes(probe, kind, bps, stages, hint, 
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+@pytest.mark.parametrize("tile,stages", [(64, 8), (2304, 3), (6144, 2), (8192, 2)])
+@pytest.mark.parametrize("tiles", [3, 601])
+def test_step_stream_probe_with_other_tile_sizes_moves_the_step_bytes(probe, tile, stages, tiles):
+    n = tiles * tile
+    params, grads, master, m, v = _streams(n, tiles + tile)
+    keep = [x.clone() for x in (master, m, v)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.mp_probe_step_streams_bulk_tile(params.data_ptr(), grads.data_ptr(), master.data_ptr(), m.data_ptr(),
+                                               v.data_ptr(), n, tile, 1, stages, 1, err.data_ptr(),
+                                               torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(params, grads)
+    for a, b in zip((master, m, v), keep):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 @pytest.mark.parametrize("bps,stages,hint", [(1, 7, 1), (2, 3, 0)])
 def test_bulk_copy_probe_copies_its_tiles(probe, bps, stages, hint):
     tile_bytes = TILE * 14
@@ -90,6 +109,11 @@ def test_bulk_probe_refuses_bad_arguments(probe):
     assert probe.mp_probe_step_streams_bulk(*args, n, 4, 7, 0, err.data_ptr(), s) != 0  # does not fit
     assert probe.mp_probe_step_streams_bulk(params[1:].data_ptr(), *args[1:], n - TILE, 1, 4, 0, err.data_ptr(),
                                             s) != 0  # unaligned
+    tile = probe.mp_probe_step_streams_bulk_tile
+    assert tile(*args, n, 0, 1, 2, 0, err.data_ptr(), s) != 0  # no tile
+    assert tile(*args, n, 96, 1, 2, 0, err.data_ptr(), s) != 0  # not a multiple of 64
+    assert tile(*args, n, 3 * TILE, 1, 2, 0, err.data_ptr(), s) != 0  # n not whole tiles
+    assert tile(*args, n, 4 * TILE, 1, 3, 0, err.data_ptr(), s) != 0  # 3 stages of 112 KB do not fit
     torch.cuda.synchronize()
     assert int(err.item()) == 0
 
