@@ -77,11 +77,10 @@ __device__ __forceinline__ double block_sum(double d, double* sh) {
 // (the TMA-staged kernel fetches a group of pieces with one bulk copy).
 // Measured on GB300 (Llama-3-8B gradients): the staged norm took 2.174-2.176
 // ms with runs of whole pieces and 2.203-2.206 ms with runs rounded only to
-// 128-B lines (better balanced, the same chained step time).
-// Shorter ranges interleave the blocks:
-// thread t of block b takes vectors b*256 + t + j*nblocks*256. Every kernel
-// of the norm uses this, so the host- and device-gradient kernels add the
-// same squares in the same order.
+// 128-B lines (better balanced, the same chained step time). Shorter ranges
+// interleave the blocks: thread t of block b takes vectors
+// b*256 + t + j*nblocks*256. Every kernel of the norm uses this, so the
+// host- and device-gradient kernels add the same squares in the same order.
 struct NormMap {
   bool contiguous;
   uint64_t first, last;  // contiguous: this block's vectors [first, last)
