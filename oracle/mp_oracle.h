@@ -23,8 +23,9 @@
  *
  * Parity unpinned: the exact 32-bit values of oracle_noise_u32. The pages
  * name SquirrelNoise5 but print no test vector, so the hash's constants and
- * shifts are pinned only by statistical tests (uniform, uncorrelated draws)
- * that a different but equally good mixer would also pass. Every other
+ * shifts are pinned only by statistical tests (uniform, uncorrelated draws,
+ * strict avalanche) that a different but equally good mixer would also
+ * pass; a dropped mixing round fails the avalanche test. Every other
  * function here is pinned by values or properties the pages or mathematics
  * fix (tests/test_oracle_pins.py).
  */

@@ -6,9 +6,12 @@ compiles it, swaps it in for the real oracle and runs the pins of
 test_oracle_pins.py until one fails. Every mutant must be caught; the
 unmodified oracle must pass them all.
 
-Not mutated: the hash's constants and shift amounts. The pages print no
-test vector for SquirrelNoise5, so those values are pinned only through the
-statistical checks, which a different but equally good mixer would pass.
+The hash is mutated only where a mistake leaves a worse mixer (a dropped
+multiply or xor-shift round), which the avalanche pin catches. Its constants
+and shift amounts, and changes that leave an equally good mixer (the seed
+xored instead of added, a shift reversed), are not: the pages print no test
+vector for SquirrelNoise5, so those are pinned only through the statistical
+checks, which a different but equally good mixer would pass.
 """
 import os
 import subprocess
@@ -103,6 +106,12 @@ MUTANTS = {
          "lr = (p <= f) ? hi : hi - (hi - lo) * (p - f) / (1.0 - f);"),
     "lr: linear decays to zero":
         ("lr = hi - (hi - lo) * p;", "lr = hi - hi * p;"),
+    "hash: final xor-shift dropped":
+        ("    bits ^= bits >> 17;\n", ""),
+    "hash: a middle multiply dropped":
+        ("    bits *= 0x6C736F4Bu;\n", ""),
+    "hash: last multiply dropped":
+        ("    bits *= 0x1B56C4F5u;\n", ""),
     "outlier: non-finite norms enter the window":
         ("    if (isfinite(x)) {\n        st->window", "    if (1) {\n        st->window"),
 }
@@ -156,6 +165,7 @@ def _pins():
         ("lr linear", P.test_lr_linear_closed_forms),
         ("lr WSD", P.test_lr_wsd_closed_forms),
         ("lr invalid", P.test_lr_rejects_invalid_arguments),
+        ("noise avalanche", P.test_noise_avalanche),
     ]
 
 
