@@ -8,9 +8,11 @@
 // host memory at the link's ~210 GB/s on GB300; but in some runs of pipelined
 // steps on some GB300 hosts, the copy engine's 16 GB took ~175 ms where SM
 // loads of the same buffer in the same process took ~92 ms. One block of 256
-// threads per SM, at a few dozen registers, fits beside the update kernel's
-// three resident blocks of 72 registers, so the copy runs concurrently with
-// the update rather than after it.
+// threads per SM, at a few dozen registers and no shared memory, fits beside
+// the update kernel's block (608 threads, 129 KB of shared memory on long
+// ranges; three blocks of 256 threads on short ones), so the copy runs
+// concurrently with the update rather than after it. Two or four blocks per
+// SM copy as fast alone but serialised with the update in a pipelined step.
 #include <cstdint>
 
 #include "mp_adamw.h"
