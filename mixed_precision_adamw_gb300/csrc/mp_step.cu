@@ -81,6 +81,10 @@ adamw_scalar_kernel(const __grid_constant__ StepArgs p, const __grid_constant__ 
 // best rate in a narrow band of tile size, consumer warps and stages, e.g.
 // with master 18 warps x 4 stages 6.78-6.81 TB/s, 17 x 4 6.65-6.68, 19 x 4
 // 6.73-6.78, 18 x 3 5.77, 18 x 5 6.36-6.50; the register path 6.65-6.67.
+// Larger tiles (two groups per consumer thread) did worse on the 8B update,
+// 33.3 ms now: 18 x 3 of 4,608 params 33.6 ms, 16 x 3 of 4,096 34.4, and two
+// stages of 4,608 or 6,144 params 52-61 ms, where the update of one tile no
+// longer overlaps the loads of the next.
 template <bool kMaster>
 struct TmaConfig {
   static constexpr int kConsumerWarps = kMaster ? 18 : 26;
