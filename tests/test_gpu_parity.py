@@ -354,8 +354,12 @@ def _norm_gpu(g: torch.Tensor, clip=1.0):
     return float(d_sumsq.item()), np.float32(d_norm.item()), np.float32(d_scale.item())
 
 
+# 2,492,429 = 16,384 x 152 + 8 x 257 + 5: on 152 SMs, just past the length from
+# which each norm block reads one contiguous run (the last runs empty), with
+# a ragged tail; (1 << 24) + 3 with a pad of 3 takes the element-wise path.
 @pytest.mark.parametrize("n,pad", [(0, 0), (1, 0), (7, 0), (8, 0), (2047, 1), (2048 * 5 + 3, 0),
-                                   (1000003, 0), (1000003, 3), (1 << 24, 0)])
+                                   (1000003, 0), (1000003, 3), (2492429, 0), (2492429, 3), (1 << 24, 0),
+                                   ((1 << 24) + 3, 3)])
 def test_grad_norm_parity(n, pad):
     rng = np.random.default_rng(n)
     g = bf16_from_f32(rng.standard_normal(n) * 10.0 ** rng.uniform(-5, 1, n))
@@ -373,9 +377,9 @@ def test_grad_norm_parity(n, pad):
 
 
 @pytest.mark.parametrize("case", ["tiny", "huge", "mixed", "zeros", "subnormal"])
-def test_grad_norm_extreme_ranges(case):
+@pytest.mark.parametrize("n", [3 * 2048 * 152 + 11, 3 * (1 << 20) + 11])  # the interleaved and the staged norm
+def test_grad_norm_extreme_ranges(case, n):
     rng = np.random.default_rng(5)
-    n = 3 * 2048 * 152 + 11
     if case == "tiny":
         x = rng.standard_normal(n) * 1e-30
     elif case == "huge":
